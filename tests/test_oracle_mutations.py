@@ -1,0 +1,163 @@
+"""Each plausible mistake planted in the oracle (on the CPU) trips a pin.
+
+The mistakes are planted by monkeypatching oracle.restore; composite
+functions look their helpers up at call time, so the planted helper is used
+throughout the restore.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import restore as R
+from tests import pins
+
+ORIG = {name: getattr(R, name) for name in
+        ("rms_norm", "layer_norm", "project", "rope_rotate_half", "rope_angles",
+         "token_placement", "restore_layer")}
+
+
+def _rope_sign_flipped(k, pos, theta):
+    return ORIG["rope_rotate_half"](k, -np.asarray(pos), theta)
+
+
+def _rope_interleaved(k, pos, theta):
+    k = np.asarray(k, np.float64)
+    dh = k.shape[-1]
+    alpha = ORIG["rope_angles"](pos, dh, theta)[:, None, :]
+    a, b = k[..., 0::2], k[..., 1::2]
+    out = np.empty_like(k)
+    out[..., 0::2] = a * np.cos(alpha) - b * np.sin(alpha)
+    out[..., 1::2] = b * np.cos(alpha) + a * np.sin(alpha)
+    return out
+
+
+def _angles_wrong_exponent(pos, head_dim, theta):
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    return np.asarray(pos, np.float64)[:, None] * np.power(theta, -i / head_dim)[None, :]
+
+
+def _rms_eps_outside(h, gamma, eps):
+    h = np.asarray(h, np.float64)
+    return h / (np.sqrt(np.mean(h * h, axis=-1, keepdims=True)) + eps) * gamma
+
+
+def _rms_no_gamma(h, gamma, eps):
+    return ORIG["rms_norm"](h, np.ones_like(np.asarray(gamma, np.float64)), eps)
+
+
+def _ln_unbiased(h, gamma, beta, eps):
+    h = np.asarray(h, np.float64)
+    mu = h.mean(axis=-1, keepdims=True)
+    var = ((h - mu) ** 2).sum(axis=-1, keepdims=True) / (h.shape[-1] - 1)
+    return (h - mu) / np.sqrt(var + eps) * gamma + beta
+
+
+def _ln_no_beta(h, gamma, beta, eps):
+    return ORIG["layer_norm"](h, gamma, np.zeros_like(np.asarray(beta, np.float64)), eps)
+
+
+def _project_transposed(x, w, b=None):
+    w = np.asarray(w, np.float64)
+    if w.shape[0] == w.shape[1]:
+        y = np.asarray(x, np.float64) @ w
+    else:   # keep shapes valid: transpose within the leading square block
+        n = min(w.shape)
+        w2 = w.copy()
+        w2[:n, :n] = w[:n, :n].T
+        y = np.asarray(x, np.float64) @ w2.T
+    return y if b is None else y + b
+
+
+def _project_no_bias(x, w, b=None):
+    return ORIG["project"](x, w, None)
+
+
+def _restore_layer_swapped(h, lw, pos, spec):
+    lw2 = R.LayerWeights(gamma=lw.gamma, beta=lw.beta, w_k=lw.w_v, w_v=lw.w_k, b_k=lw.b_v,
+                         b_v=lw.b_k)
+    return ORIG["restore_layer"](h, lw2, pos, spec)
+
+
+def _restore_layer_pos_off_by_one(h, lw, pos, spec):
+    return ORIG["restore_layer"](h, lw, np.asarray(pos) + 1, spec)
+
+
+def _restore_layer_rope_on_v(h, lw, pos, spec):
+    k, v = ORIG["restore_layer"](h, lw, pos, spec)
+    if spec.rope:
+        v = ORIG["rope_rotate_half"](v, pos, spec.rope_theta)
+    return k, v
+
+
+def _placement_offset_from_start(cu_seqlens, start_pos, block_table, block_size, num_blocks=None):
+    # mistake: offset within the block taken from the token index, not the position
+    pl = ORIG["token_placement"](cu_seqlens, start_pos, block_table, block_size, num_blocks)
+    cu = np.asarray(cu_seqlens)
+    idx = pl.pos - np.asarray(start_pos)[pl.request]
+    pl.slot = (pl.slot // block_size) * block_size + idx % block_size
+    return pl
+
+
+def _placement_block_from_index(cu_seqlens, start_pos, block_table, block_size, num_blocks=None):
+    # mistake: logical block from the token index within the request, ignoring start
+    pl = ORIG["token_placement"](cu_seqlens, start_pos, block_table, block_size, num_blocks)
+    bt = np.asarray(block_table)
+    idx = pl.pos - np.asarray(start_pos)[pl.request]
+    pl.slot = bt[pl.request, idx // block_size] * block_size + pl.pos % block_size
+    return pl
+
+
+def _facts():
+    with open(os.path.join(os.path.dirname(__file__), "golden", "kv_capacity_a100.json")) as f:
+        return json.load(f)
+
+
+def _all_pins():
+    yield pins.pin_rms_constant, (R,)
+    yield pins.pin_rms_values, (R,)
+    yield pins.pin_layer_norm, (R,)
+    yield pins.pin_project_bruteforce, (R,)
+    yield pins.pin_rope_closed_form, (R,)
+    yield pins.pin_rope_invariants, (R,)
+    yield pins.pin_placement, (R,)
+    yield pins.pin_identity_weights, (R,)
+    yield pins.pin_tiny_forward, (R, "llama")
+    yield pins.pin_tiny_forward, (R, "opt")
+
+
+MUTANTS = [
+    ("rope_rotate_half", _rope_sign_flipped),
+    ("rope_rotate_half", _rope_interleaved),
+    ("rope_angles", _angles_wrong_exponent),
+    ("rms_norm", _rms_eps_outside),
+    ("rms_norm", _rms_no_gamma),
+    ("layer_norm", _ln_unbiased),
+    ("layer_norm", _ln_no_beta),
+    ("project", _project_transposed),
+    ("project", _project_no_bias),
+    ("restore_layer", _restore_layer_swapped),
+    ("restore_layer", _restore_layer_pos_off_by_one),
+    ("restore_layer", _restore_layer_rope_on_v),
+    ("token_placement", _placement_offset_from_start),
+    ("token_placement", _placement_block_from_index),
+]
+
+
+@pytest.mark.parametrize("attr,mutant", MUTANTS, ids=[m.__name__.strip("_") for _, m in MUTANTS])
+def test_planted_mistake_is_caught(monkeypatch, attr, mutant):
+    monkeypatch.setattr(R, attr, mutant)
+    failed = []
+    for pin, args in _all_pins():
+        try:
+            pin(*args)
+        except (AssertionError, ValueError, IndexError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught the planted mistake {mutant.__name__}"
+
+
+def test_unmutated_oracle_passes_every_pin():
+    for pin, args in _all_pins():
+        pin(*args)
+    pins.pin_kv_bytes(R, _facts())

@@ -1,0 +1,216 @@
+/*
+ * hcr.h -- restore an attention KV cache from saved per-layer hidden states.
+ *
+ * The operation (HCache episode, "Fast State Restoration for Evicted LLM KV
+ * Caches", cue 14): instead of keeping an evicted request's K and V, keep
+ * each layer's input hidden state H (cue 3: the layer input, the embedding
+ * output for the first layer) and rebuild the cache by running only the
+ * key/value projections, K = W_k H and V = W_v H; attention and the FFN are
+ * skipped.  A restore reads every token of one layer together (cue 16) and
+ * many requests' tokens are projected together so the GEMM shape stays
+ * regular (cue 20).
+ *
+ * This library adds what a pre-norm transformer needs around that
+ * projection: the layer's input norm (RMSNorm with gamma, or LayerNorm with
+ * gamma/beta), optional K/V biases, rotate-half RoPE on K at each token's
+ * absolute position, and a paged cache addressed through a block table.
+ *
+ * For each layer l in [layer_begin, layer_end) and each restored token t of
+ * request r at position p:
+ *     x      = norm_l(H_l[t])                         (RMSNorm or LayerNorm)
+ *     k      = x W_k[l]^T (+ b_k[l]),   v = x W_v[l]^T (+ b_v[l])
+ *     k      = RoPE(k, p)  per head: pairs (i, i+dh/2) turn by p*theta^(-2i/dh)
+ *     slot   = block_table[r][p / B] * B + p % B
+ *     k_cache[l][slot] = k,   v_cache[l][slot] = v      (rounded to nearest even)
+ *
+ * Numbers: inputs and outputs are bf16 or fp16 (one type per handle); the
+ * projection accumulates in fp32 on the tensor cores; norm statistics, bias,
+ * RoPE and the cast run in fp32.  gamma is folded into the packed weights
+ * (W' = [W_k; W_v] diag(gamma), rounded once to the storage type), so the
+ * norm is applied as a per-row scale after the GEMM.
+ *
+ * Threading and streams: a handle is immutable after hcr_create and may be
+ * used from several host threads and streams at once, provided each
+ * concurrent restore has its own workspace.  Every call that takes a stream
+ * only enqueues work on it; it does not synchronise unless stated.
+ *
+ * All entry points return hcr_status.  Host-side argument errors are
+ * reported before any work is enqueued, and hcr_last_error() then returns a
+ * message naming the offending argument.
+ */
+#ifndef HCR_H_
+#define HCR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HCR_OK = 0,
+  HCR_ERR_INVALID_ARG = 1,   /* a host argument is null, out of range or inconsistent      */
+  HCR_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head_dim not 64/128/256)   */
+  HCR_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (no device, launch, ...) */
+  HCR_ERR_OOM = 4,           /* device allocation inside hcr_create failed                  */
+  HCR_ERR_WORKSPACE = 5,     /* workspace pointer null/misaligned or smaller than needed    */
+  HCR_ERR_DEVICE_BOUNDS = 6, /* (device) a block id, logical block or position was out of
+                                range; the affected rows were skipped, nothing else written */
+  HCR_ERR_TIMEOUT = 7        /* (device) a pipeline wait exceeded its time limit; the kernel
+                                stopped early and released its resources                   */
+} hcr_status;
+
+enum { HCR_NORM_RMS = 0, HCR_NORM_LAYER = 1 };
+enum { HCR_ROPE_NONE = 0, HCR_ROPE_ROTATE_HALF = 1 };
+enum { HCR_DTYPE_BF16 = 0, HCR_DTYPE_FP16 = 1 };
+
+/* Device error bits accumulated by the kernels (see hcr_check_device_error). */
+enum {
+  HCR_DEVERR_BLOCK_ID = 1u << 0,     /* block_table entry < 0 or >= num_blocks           */
+  HCR_DEVERR_LOGICAL_BLOCK = 1u << 1,/* position / B >= max_blocks_per_req               */
+  HCR_DEVERR_POSITION = 1u << 2,     /* start_pos < 0, or position >= max_position (RoPE) */
+  HCR_DEVERR_SEQLENS = 1u << 3,      /* cu_seqlens not non-decreasing from 0 to n_tokens */
+  HCR_DEVERR_TIMEOUT = 1u << 4       /* a bounded pipeline wait gave up                  */
+};
+
+/* Model dimensions, fixed at hcr_create. */
+typedef struct {
+  int32_t n_layers;      /* layers whose parameters the handle holds                       */
+  int32_t d_model;       /* width of the hidden state; multiple of 8                       */
+  int32_t n_heads;       /* query heads (only checked: multiple of n_kv_heads)             */
+  int32_t n_kv_heads;    /* key/value heads; n_kv_heads < n_heads is grouped-query attn.   */
+  int32_t head_dim;      /* 64, 128 or 256                                                 */
+  int32_t norm;          /* HCR_NORM_RMS or HCR_NORM_LAYER                                 */
+  float norm_eps;        /* added to the mean square (RMS) or variance (LN) inside the sqrt */
+  int32_t rope;          /* HCR_ROPE_NONE or HCR_ROPE_ROTATE_HALF                          */
+  float rope_theta;      /* RoPE base, e.g. 10000                                          */
+  int32_t max_position;  /* RoPE positions supported: 0 .. max_position-1 (table size)     */
+  int32_t dtype;         /* HCR_DTYPE_BF16 or HCR_DTYPE_FP16: weights, hidden and cache    */
+  int32_t has_kv_bias;   /* nonzero: b_k and b_v are given                                 */
+} hcr_model_dims;
+
+/* Paged cache geometry.  k_cache and v_cache are each laid out as
+ *   [layer][num_blocks][block_size][n_kv_heads][head_dim]
+ * with layer_stride_elems elements between consecutive layers (0 means the
+ * dense stride num_blocks*block_size*n_kv_heads*head_dim). */
+typedef struct {
+  int32_t num_blocks;
+  int32_t block_size;
+  int64_t layer_stride_elems;
+} hcr_cache_layout;
+
+typedef struct hcr_handle hcr_handle;
+
+/*
+ * hcr_create -- pack one model's restore parameters on the current device.
+ *
+ * gamma, w_k, w_v: host arrays of n_layers DEVICE pointers, in the dims'
+ * dtype: gamma[l] [d_model]; w_k[l], w_v[l] [n_kv_heads*head_dim][d_model]
+ * row-major (PyTorch Linear layout, K = X W_k^T).  beta: same, [d_model],
+ * required for HCR_NORM_LAYER, must be NULL for RMS.  b_k, b_v: [n_kv*dh],
+ * required iff has_kv_bias, else NULL.
+ *
+ * The caller keeps ownership of its parameters and may free them once this
+ * returns; the handle owns packed copies: W' = [W_k; W_v] diag(gamma) in the
+ * storage dtype, per-column fp32 constants (LayerNorm column sums and the
+ * folded bias W beta + b), an fp32 RoPE cos/sin table built in fp64 on the
+ * host, and a device error word.  Synchronises the device before returning.
+ * Errors: HCR_ERR_INVALID_ARG, HCR_ERR_UNSUPPORTED, HCR_ERR_CUDA, HCR_ERR_OOM;
+ * *out is set to NULL on error.
+ */
+hcr_status hcr_create(const hcr_model_dims* dims, const void* const* gamma,
+                      const void* const* beta, const void* const* w_k,
+                      const void* const* w_v, const void* const* b_k,
+                      const void* const* b_v, hcr_handle** out);
+
+/* Releases everything the handle owns.  Synchronises the device.  NULL is a no-op. */
+void hcr_destroy(hcr_handle* h);
+
+/*
+ * hcr_workspace_bytes -- device scratch a restore of n_tokens tokens over
+ * n_layers_in_range layers needs (per-token slot and position, per-row norm
+ * statistics).  Returns 0 for invalid arguments or an empty restore.
+ */
+size_t hcr_workspace_bytes(const hcr_handle* h, int32_t n_tokens, int32_t n_layers_in_range);
+
+/*
+ * hcr_restore -- restore layers [layer_begin, layer_end) of n_req requests.
+ *
+ * hidden:      DEVICE [layer_end-layer_begin][n_tokens][d_model], dtype of the
+ *              handle, 16-byte aligned.  Row t is the t-th token of the
+ *              requests concatenated in order (HCache episode, cue 16: one
+ *              layer's tokens are read together).
+ * n_req, n_tokens: host values; n_tokens must equal cu_seqlens[n_req].
+ * cu_seqlens:  DEVICE int32 [n_req+1], cu_seqlens[0] = 0, non-decreasing;
+ *              request r owns rows cu_seqlens[r] .. cu_seqlens[r+1]-1.
+ * start_pos:   DEVICE int32 [n_req]; row cu_seqlens[r]+i sits at absolute
+ *              position start_pos[r]+i.  Positions below start_pos[r] are a
+ *              resident prefix and are never written.
+ * block_table: DEVICE int32 [n_req][max_blocks_per_req]; entry [r][b] is the
+ *              physical block holding positions b*B .. b*B+B-1 of request r.
+ * k_cache, v_cache: DEVICE, base of layer layer_begin, laid out as
+ *              hcr_cache_layout says, 16-byte aligned.  Only the slots of the
+ *              restored positions are written; every other byte is untouched.
+ * workspace:   DEVICE, >= hcr_workspace_bytes(h, n_tokens, layers), 256-byte
+ *              aligned, owned by the caller, not shared with a concurrent call.
+ * stream:      a cudaStream_t (NULL = legacy default stream).
+ *
+ * Enqueues two kernels (hcr_restore_prepare, then hcr_restore_project) and
+ * returns.  n_tokens == 0 or an empty layer range enqueues nothing.
+ * Distinct requests must not share physical blocks (the result is then
+ * undefined).  Out-of-range block ids or positions found on the device skip
+ * the affected rows and set error bits; read them with
+ * hcr_check_device_error.
+ */
+hcr_status hcr_restore(hcr_handle* h, const void* hidden, int32_t layer_begin,
+                       int32_t layer_end, int32_t n_req, int32_t n_tokens,
+                       const int32_t* cu_seqlens, const int32_t* start_pos,
+                       const int32_t* block_table, int32_t max_blocks_per_req,
+                       void* k_cache, void* v_cache, const hcr_cache_layout* layout,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * hcr_restore_prepare / hcr_restore_project -- the two stages of hcr_restore,
+ * with identical arguments.  prepare maps every token to its (position,
+ * slot) and computes each (layer, token) row's norm statistics into the
+ * workspace; project runs the fused K||V GEMM with the norm, bias, RoPE,
+ * cast and paged scatter in its epilogue, reading that workspace.  Calling
+ * prepare then project on one stream with the same arguments is exactly
+ * hcr_restore; splitting them lets a caller time or overlap the stages.
+ */
+hcr_status hcr_restore_prepare(hcr_handle* h, const void* hidden, int32_t layer_begin,
+                               int32_t layer_end, int32_t n_req, int32_t n_tokens,
+                               const int32_t* cu_seqlens, const int32_t* start_pos,
+                               const int32_t* block_table, int32_t max_blocks_per_req,
+                               void* k_cache, void* v_cache, const hcr_cache_layout* layout,
+                               void* workspace, size_t workspace_bytes, void* stream);
+hcr_status hcr_restore_project(hcr_handle* h, const void* hidden, int32_t layer_begin,
+                               int32_t layer_end, int32_t n_req, int32_t n_tokens,
+                               const int32_t* cu_seqlens, const int32_t* start_pos,
+                               const int32_t* block_table, int32_t max_blocks_per_req,
+                               void* k_cache, void* v_cache, const hcr_cache_layout* layout,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * hcr_check_device_error -- synchronise `stream`, then read and clear the
+ * handle's device error word.  Returns HCR_OK, HCR_ERR_DEVICE_BOUNDS or
+ * HCR_ERR_TIMEOUT (timeout wins), or HCR_ERR_CUDA if the synchronisation
+ * failed.  The raw HCR_DEVERR_* bits go to *flags when flags is not NULL.
+ */
+hcr_status hcr_check_device_error(hcr_handle* h, void* stream, uint32_t* flags);
+
+/* Static description of a status code. */
+const char* hcr_status_string(hcr_status s);
+
+/* Message for the most recent error returned on the calling host thread. */
+const char* hcr_last_error(void);
+
+/* Number of SMs the handle's persistent kernel is sized for (diagnostics). */
+int32_t hcr_num_sms(const hcr_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HCR_H_ */

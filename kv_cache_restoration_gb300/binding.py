@@ -1,0 +1,196 @@
+"""ctypes binding of libhcr.so: the C ABI of include/hcr.h under the same names.
+
+Argument marshalling only -- every step of a restore runs in the library's
+CUDA kernels.  Tensors are passed by their device pointers; the library
+never sees a torch type.  There is no CPU fallback: if libhcr.so is missing,
+importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+from .build import LIB
+
+HCR_OK = 0
+HCR_ERR_INVALID_ARG = 1
+HCR_ERR_UNSUPPORTED = 2
+HCR_ERR_CUDA = 3
+HCR_ERR_OOM = 4
+HCR_ERR_WORKSPACE = 5
+HCR_ERR_DEVICE_BOUNDS = 6
+HCR_ERR_TIMEOUT = 7
+
+HCR_NORM_RMS, HCR_NORM_LAYER = 0, 1
+HCR_ROPE_NONE, HCR_ROPE_ROTATE_HALF = 0, 1
+HCR_DTYPE_BF16, HCR_DTYPE_FP16 = 0, 1
+
+HCR_DEVERR_BLOCK_ID = 1 << 0
+HCR_DEVERR_LOGICAL_BLOCK = 1 << 1
+HCR_DEVERR_POSITION = 1 << 2
+HCR_DEVERR_SEQLENS = 1 << 3
+HCR_DEVERR_TIMEOUT = 1 << 4
+
+
+class hcr_model_dims(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("d_model", ctypes.c_int32),
+                ("n_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("norm", ctypes.c_int32),
+                ("norm_eps", ctypes.c_float), ("rope", ctypes.c_int32),
+                ("rope_theta", ctypes.c_float), ("max_position", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("has_kv_bias", ctypes.c_int32)]
+
+
+class hcr_cache_layout(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("layer_stride_elems", ctypes.c_int64)]
+
+
+class HcrError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str):
+        super().__init__(f"{where}: {message}")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB):
+        raise ImportError(
+            f"{LIB} is missing: the CUDA library must be built first "
+            "(python -m kv_cache_restoration_gb300.build); there is no CPU fallback")
+    return ctypes.CDLL(LIB)
+
+
+lib = _load()
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_RESTORE_ARGTYPES = [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _vp,
+                     ctypes.POINTER(hcr_cache_layout), _vp, ctypes.c_size_t, _vp]
+
+lib.hcr_create.argtypes = [ctypes.POINTER(hcr_model_dims)] + [ctypes.POINTER(_vp)] * 6 + [
+    ctypes.POINTER(_vp)]
+lib.hcr_create.restype = ctypes.c_int
+lib.hcr_destroy.argtypes = [_vp]
+lib.hcr_destroy.restype = None
+lib.hcr_workspace_bytes.argtypes = [_vp, _i32, _i32]
+lib.hcr_workspace_bytes.restype = ctypes.c_size_t
+for _name in ("hcr_restore", "hcr_restore_prepare", "hcr_restore_project"):
+    getattr(lib, _name).argtypes = _RESTORE_ARGTYPES
+    getattr(lib, _name).restype = ctypes.c_int
+lib.hcr_check_device_error.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]
+lib.hcr_check_device_error.restype = ctypes.c_int
+lib.hcr_status_string.argtypes = [ctypes.c_int]
+lib.hcr_status_string.restype = ctypes.c_char_p
+lib.hcr_last_error.argtypes = []
+lib.hcr_last_error.restype = ctypes.c_char_p
+lib.hcr_num_sms.argtypes = [_vp]
+lib.hcr_num_sms.restype = _i32
+
+
+def hcr_status_string(status: int) -> str:
+    return lib.hcr_status_string(status).decode()
+
+
+def hcr_last_error() -> str:
+    return lib.hcr_last_error().decode()
+
+
+def _check(status: int, where: str) -> int:
+    if status != HCR_OK:
+        raise HcrError(status, where, f"{hcr_status_string(status)} -- {hcr_last_error()}")
+    return status
+
+
+def _ptr(x) -> Optional[int]:
+    """Device (or host) address of a tensor, an int address, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _ptr_array(xs: Optional[Sequence]):
+    if xs is None:
+        return None
+    arr = (_vp * len(xs))(*[_ptr(x) for x in xs])
+    return arr
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream   # torch.cuda.Stream
+
+
+def hcr_create(dims: hcr_model_dims, gamma, beta, w_k, w_v, b_k=None, b_v=None, *,
+               check: bool = True):
+    """Returns (status, handle address or None).  Raises HcrError if check and status != OK."""
+    out = _vp()
+    arrays = [_ptr_array(x) for x in (gamma, beta, w_k, w_v, b_k, b_v)]
+    casted = [ctypes.cast(a, ctypes.POINTER(_vp)) if a is not None else None for a in arrays]
+    st = lib.hcr_create(ctypes.byref(dims), *casted, ctypes.byref(out))
+    if check:
+        _check(st, "hcr_create")
+    return st, out.value
+
+
+def hcr_destroy(handle) -> None:
+    lib.hcr_destroy(handle)
+
+
+def hcr_workspace_bytes(handle, n_tokens: int, n_layers_in_range: int) -> int:
+    return lib.hcr_workspace_bytes(handle, n_tokens, n_layers_in_range)
+
+
+def _restore_call(fn, name, handle, hidden, layer_begin, layer_end, n_req, n_tokens, cu_seqlens,
+                  start_pos, block_table, max_blocks_per_req, k_cache, v_cache, layout,
+                  workspace, workspace_bytes, stream, check):
+    st = fn(handle, _ptr(hidden), layer_begin, layer_end, n_req, n_tokens, _ptr(cu_seqlens),
+            _ptr(start_pos), _ptr(block_table), max_blocks_per_req, _ptr(k_cache),
+            _ptr(v_cache), ctypes.byref(layout) if layout is not None else None,
+            _ptr(workspace), workspace_bytes, _stream_ptr(stream))
+    if check:
+        _check(st, name)
+    return st
+
+
+def hcr_restore(handle, hidden, layer_begin, layer_end, n_req, n_tokens, cu_seqlens, start_pos,
+                block_table, max_blocks_per_req, k_cache, v_cache, layout, workspace,
+                workspace_bytes, stream=None, *, check: bool = True) -> int:
+    return _restore_call(lib.hcr_restore, "hcr_restore", handle, hidden, layer_begin, layer_end,
+                         n_req, n_tokens, cu_seqlens, start_pos, block_table,
+                         max_blocks_per_req, k_cache, v_cache, layout, workspace,
+                         workspace_bytes, stream, check)
+
+
+def hcr_restore_prepare(handle, hidden, layer_begin, layer_end, n_req, n_tokens, cu_seqlens,
+                        start_pos, block_table, max_blocks_per_req, k_cache, v_cache, layout,
+                        workspace, workspace_bytes, stream=None, *, check: bool = True) -> int:
+    return _restore_call(lib.hcr_restore_prepare, "hcr_restore_prepare", handle, hidden,
+                         layer_begin, layer_end, n_req, n_tokens, cu_seqlens, start_pos,
+                         block_table, max_blocks_per_req, k_cache, v_cache, layout, workspace,
+                         workspace_bytes, stream, check)
+
+
+def hcr_restore_project(handle, hidden, layer_begin, layer_end, n_req, n_tokens, cu_seqlens,
+                        start_pos, block_table, max_blocks_per_req, k_cache, v_cache, layout,
+                        workspace, workspace_bytes, stream=None, *, check: bool = True) -> int:
+    return _restore_call(lib.hcr_restore_project, "hcr_restore_project", handle, hidden,
+                         layer_begin, layer_end, n_req, n_tokens, cu_seqlens, start_pos,
+                         block_table, max_blocks_per_req, k_cache, v_cache, layout, workspace,
+                         workspace_bytes, stream, check)
+
+
+def hcr_check_device_error(handle, stream=None):
+    """Returns (status, raw HCR_DEVERR_* bits); never raises for device errors."""
+    flags = ctypes.c_uint32(0)
+    st = lib.hcr_check_device_error(handle, _stream_ptr(stream), ctypes.byref(flags))
+    return st, flags.value
+
+
+def hcr_num_sms(handle) -> int:
+    return lib.hcr_num_sms(handle)

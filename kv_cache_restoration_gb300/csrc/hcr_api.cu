@@ -1,0 +1,471 @@
+// Host side of the C ABI declared in include/hcr.h: argument validation,
+// handle construction (weight packing, RoPE table), workspace planning,
+// TMA tensor-map encoding and kernel launches.  No host code here touches
+// restore data; every step of the computation runs in the CUDA kernels.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "hcr_internal.h"
+
+namespace hcr {
+namespace {
+
+thread_local std::string g_last_error;
+
+hcr_status fail(hcr_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+hcr_status cuda_fail(cudaError_t e, const char* what) {
+  cudaGetLastError();  // clear a sticky-free error so later calls start clean
+  return fail(e == cudaErrorMemoryAllocation ? HCR_ERR_OOM : HCR_ERR_CUDA, "%s: %s (%s)", what,
+              cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so the
+// library needs no link-time dependency on libcuda.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D K-major operand map: dims (inner, rows, layers), box (64, box_rows, 1),
+// 128-byte swizzle, zero fill outside the tensor.
+hcr_status encode_3d(CUtensorMap* map, const void* base, int dtype, uint64_t inner, uint64_t rows,
+                     uint64_t layers, uint32_t box_rows, const char* what) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(HCR_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[3] = {inner, rows, layers};
+  const cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+  const cuuint32_t box[3] = {uint32_t(kBlockK), box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map,
+                  dtype == HCR_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(HCR_ERR_CUDA, "tensor map for %s: CUresult %d", what, int(r));
+  return HCR_OK;
+}
+
+hcr_status validate_dims(const hcr_model_dims* d) {
+  if (!d) return fail(HCR_ERR_INVALID_ARG, "dims is NULL");
+  if (d->n_layers < 1) return fail(HCR_ERR_INVALID_ARG, "n_layers must be >= 1");
+  if (d->d_model < 8 || d->d_model % 8)
+    return fail(HCR_ERR_INVALID_ARG, "d_model must be a positive multiple of 8");
+  if (d->n_kv_heads < 1 || d->n_heads < d->n_kv_heads || d->n_heads % d->n_kv_heads)
+    return fail(HCR_ERR_INVALID_ARG, "n_heads must be a positive multiple of n_kv_heads");
+  if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256)
+    return fail(HCR_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
+  if (int64_t(d->n_kv_heads) * d->head_dim > (1 << 20))
+    return fail(HCR_ERR_UNSUPPORTED, "n_kv_heads * head_dim too large");
+  if (d->norm != HCR_NORM_RMS && d->norm != HCR_NORM_LAYER)
+    return fail(HCR_ERR_INVALID_ARG, "norm must be HCR_NORM_RMS or HCR_NORM_LAYER");
+  if (!(d->norm_eps >= 0.f) || !std::isfinite(d->norm_eps))
+    return fail(HCR_ERR_INVALID_ARG, "norm_eps must be finite and >= 0");
+  if (d->rope != HCR_ROPE_NONE && d->rope != HCR_ROPE_ROTATE_HALF)
+    return fail(HCR_ERR_INVALID_ARG, "rope must be HCR_ROPE_NONE or HCR_ROPE_ROTATE_HALF");
+  if (d->rope) {
+    if (!(d->rope_theta > 0.f) || !std::isfinite(d->rope_theta))
+      return fail(HCR_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+    if (d->max_position < 1 || d->max_position > (1 << 24))
+      return fail(HCR_ERR_INVALID_ARG, "max_position must be in [1, 2^24]");
+  }
+  if (d->dtype != HCR_DTYPE_BF16 && d->dtype != HCR_DTYPE_FP16)
+    return fail(HCR_ERR_INVALID_ARG, "dtype must be HCR_DTYPE_BF16 or HCR_DTYPE_FP16");
+  return HCR_OK;
+}
+
+struct RestoreArgs {
+  const void* hidden;
+  int32_t layer_begin, layer_end, n_req, n_tokens;
+  const int32_t *cu_seqlens, *start_pos, *block_table;
+  int32_t max_blocks;
+  void *k_cache, *v_cache;
+  const hcr_cache_layout* layout;
+  void* workspace;
+  size_t workspace_bytes;
+  cudaStream_t stream;
+};
+
+// Returns HCR_OK with *empty set when there is nothing to do.
+hcr_status validate_restore(const hcr_handle* h, const RestoreArgs& a, bool* empty) {
+  *empty = false;
+  if (!h) return fail(HCR_ERR_INVALID_ARG, "handle is NULL");
+  const hcr_model_dims& d = h->impl.dims;
+  if (a.layer_begin < 0 || a.layer_end < a.layer_begin || a.layer_end > d.n_layers)
+    return fail(HCR_ERR_INVALID_ARG, "layer range [%d, %d) outside [0, %d)", a.layer_begin,
+                a.layer_end, d.n_layers);
+  if (a.n_tokens < 0) return fail(HCR_ERR_INVALID_ARG, "n_tokens must be >= 0");
+  if (a.n_req < 0) return fail(HCR_ERR_INVALID_ARG, "n_req must be >= 0");
+  if (a.n_tokens == 0 || a.layer_end == a.layer_begin) {
+    *empty = true;
+    return HCR_OK;
+  }
+  if (a.n_req < 1) return fail(HCR_ERR_INVALID_ARG, "n_tokens > 0 needs n_req >= 1");
+  if (!a.hidden) return fail(HCR_ERR_INVALID_ARG, "hidden is NULL");
+  if (!aligned(a.hidden, 16)) return fail(HCR_ERR_INVALID_ARG, "hidden must be 16-byte aligned");
+  if (!a.cu_seqlens || !a.start_pos || !a.block_table)
+    return fail(HCR_ERR_INVALID_ARG, "cu_seqlens, start_pos and block_table must be non-NULL");
+  if (a.max_blocks < 1) return fail(HCR_ERR_INVALID_ARG, "max_blocks_per_req must be >= 1");
+  if (!a.k_cache || !a.v_cache) return fail(HCR_ERR_INVALID_ARG, "k_cache/v_cache is NULL");
+  if (!aligned(a.k_cache, 16) || !aligned(a.v_cache, 16))
+    return fail(HCR_ERR_INVALID_ARG, "k_cache and v_cache must be 16-byte aligned");
+  if (!a.layout) return fail(HCR_ERR_INVALID_ARG, "layout is NULL");
+  if (a.layout->num_blocks < 1 || a.layout->block_size < 1)
+    return fail(HCR_ERR_INVALID_ARG, "num_blocks and block_size must be >= 1");
+  const int64_t row = int64_t(d.n_kv_heads) * d.head_dim;
+  const int64_t dense = int64_t(a.layout->num_blocks) * a.layout->block_size * row;
+  if (a.layout->layer_stride_elems != 0 && a.layout->layer_stride_elems < dense)
+    return fail(HCR_ERR_INVALID_ARG, "layer_stride_elems %lld smaller than one layer (%lld)",
+                (long long)a.layout->layer_stride_elems, (long long)dense);
+  if (a.layout->layer_stride_elems % 8)
+    return fail(HCR_ERR_INVALID_ARG, "layer_stride_elems must be a multiple of 8");
+  const size_t need =
+      workspace_layout(a.n_tokens, a.layer_end - a.layer_begin, d.norm == HCR_NORM_LAYER).total;
+  if (!a.workspace) return fail(HCR_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(a.workspace, 256))
+    return fail(HCR_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (a.workspace_bytes < need)
+    return fail(HCR_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", a.workspace_bytes, need);
+  return HCR_OK;
+}
+
+hcr_status do_prepare(hcr_handle* h, const RestoreArgs& a) {
+  const Handle& H = h->impl;
+  const hcr_model_dims& d = H.dims;
+  const int32_t nl = a.layer_end - a.layer_begin;
+  const WorkspaceLayout w = workspace_layout(a.n_tokens, nl, d.norm == HCR_NORM_LAYER);
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  PrepareParams p{};
+  p.cu_seqlens = a.cu_seqlens;
+  p.start_pos = a.start_pos;
+  p.block_table = a.block_table;
+  p.n_req = a.n_req;
+  p.n_tokens = a.n_tokens;
+  p.max_blocks = a.max_blocks;
+  p.num_blocks = a.layout->num_blocks;
+  p.block_size = a.layout->block_size;
+  p.max_position = d.max_position;
+  p.check_position = d.rope != HCR_ROPE_NONE;
+  p.slot = reinterpret_cast<int64_t*>(ws + w.slot_off);
+  p.pos = reinterpret_cast<int32_t*>(ws + w.pos_off);
+  p.hidden = a.hidden;
+  p.n_layers = nl;
+  p.d_model = d.d_model;
+  p.layer_norm = d.norm == HCR_NORM_LAYER;
+  p.dtype = d.dtype;
+  p.eps = d.norm_eps;
+  p.rstd = reinterpret_cast<float*>(ws + w.rstd_off);
+  p.mean = p.layer_norm ? reinterpret_cast<float*>(ws + w.mean_off) : nullptr;
+  p.err = H.err;
+  cudaError_t e = launch_prepare(p, a.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "prepare launch");
+  return HCR_OK;
+}
+
+hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
+  const Handle& H = h->impl;
+  const hcr_model_dims& d = H.dims;
+  const int32_t nl = a.layer_end - a.layer_begin;
+  const WorkspaceLayout w = workspace_layout(a.n_tokens, nl, d.norm == HCR_NORM_LAYER);
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  const int32_t d_kv = d.n_kv_heads * d.head_dim;
+
+  CUtensorMap tmap_h;
+  hcr_status st = encode_3d(&tmap_h, a.hidden, d.dtype, uint64_t(d.d_model),
+                            uint64_t(a.n_tokens), uint64_t(nl), kBlockM, "hidden");
+  if (st != HCR_OK) return st;
+
+  ProjectParams p{};
+  p.n_tokens = a.n_tokens;
+  p.d_model = d.d_model;
+  p.n_cols = 2 * d_kv;
+  p.d_kv = d_kv;
+  p.head_dim = d.head_dim;
+  p.n_layers = nl;
+  p.layer_begin = a.layer_begin;
+  p.m_tiles = (a.n_tokens + kBlockM - 1) / kBlockM;
+  p.n_tiles = (2 * d_kv + kBlockN - 1) / kBlockN;
+  p.k_blocks = (d.d_model + kBlockK - 1) / kBlockK;
+  p.num_tiles = int64_t(nl) * p.m_tiles * p.n_tiles;
+  p.layer_norm = d.norm == HCR_NORM_LAYER;
+  p.has_bias = H.col_bias != nullptr;
+  p.rope = d.rope != HCR_ROPE_NONE;
+  p.dtype = d.dtype;
+  p.slot = reinterpret_cast<const int64_t*>(ws + w.slot_off);
+  p.pos = reinterpret_cast<const int32_t*>(ws + w.pos_off);
+  p.rstd = reinterpret_cast<const float*>(ws + w.rstd_off);
+  p.mean = p.layer_norm ? reinterpret_cast<const float*>(ws + w.mean_off) : nullptr;
+  p.col_sum = H.col_sum ? H.col_sum + int64_t(a.layer_begin) * 2 * d_kv : nullptr;
+  p.col_bias = H.col_bias ? H.col_bias + int64_t(a.layer_begin) * 2 * d_kv : nullptr;
+  p.rope_tab = H.rope_tab;
+  p.k_cache = a.k_cache;
+  p.v_cache = a.v_cache;
+  const int64_t row = int64_t(d_kv);
+  p.layer_stride = a.layout->layer_stride_elems
+                       ? a.layout->layer_stride_elems
+                       : int64_t(a.layout->num_blocks) * a.layout->block_size * row;
+  p.row_elems = d_kv;
+  p.err = H.err;
+  p.debug_stall = H.debug_stall;
+  const int grid = int(std::min<int64_t>(p.num_tiles, H.num_sms));
+  cudaError_t e = launch_project(tmap_h, H.tmap_w, p, grid, a.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "project launch");
+  return HCR_OK;
+}
+
+void free_handle(Handle& H) {
+  cudaFree(H.w_packed);
+  cudaFree(H.col_sum);
+  cudaFree(H.col_bias);
+  cudaFree(H.rope_tab);
+  cudaFree(H.err);
+  H.w_packed = nullptr;
+  H.col_sum = H.col_bias = nullptr;
+  H.rope_tab = nullptr;
+  H.err = nullptr;
+}
+
+}  // namespace
+}  // namespace hcr
+
+using namespace hcr;
+
+extern "C" {
+
+const char* hcr_status_string(hcr_status s) {
+  switch (s) {
+    case HCR_OK: return "HCR_OK";
+    case HCR_ERR_INVALID_ARG: return "HCR_ERR_INVALID_ARG: invalid argument";
+    case HCR_ERR_UNSUPPORTED: return "HCR_ERR_UNSUPPORTED: unsupported configuration";
+    case HCR_ERR_CUDA: return "HCR_ERR_CUDA: CUDA call failed";
+    case HCR_ERR_OOM: return "HCR_ERR_OOM: device allocation failed";
+    case HCR_ERR_WORKSPACE: return "HCR_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case HCR_ERR_DEVICE_BOUNDS:
+      return "HCR_ERR_DEVICE_BOUNDS: out-of-range block id or position; rows skipped";
+    case HCR_ERR_TIMEOUT: return "HCR_ERR_TIMEOUT: device pipeline wait timed out";
+  }
+  return "unknown hcr_status";
+}
+
+const char* hcr_last_error(void) { return g_last_error.c_str(); }
+
+hcr_status hcr_create(const hcr_model_dims* dims, const void* const* gamma,
+                      const void* const* beta, const void* const* w_k, const void* const* w_v,
+                      const void* const* b_k, const void* const* b_v, hcr_handle** out) {
+  if (!out) return fail(HCR_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  hcr_status st = validate_dims(dims);
+  if (st != HCR_OK) return st;
+  const hcr_model_dims& d = *dims;
+  const bool ln = d.norm == HCR_NORM_LAYER;
+  if (!gamma || !w_k || !w_v) return fail(HCR_ERR_INVALID_ARG, "gamma, w_k, w_v must be given");
+  if (ln && !beta) return fail(HCR_ERR_INVALID_ARG, "LayerNorm needs beta");
+  if (!ln && beta) return fail(HCR_ERR_INVALID_ARG, "RMSNorm takes no beta (pass NULL)");
+  if (d.has_kv_bias && (!b_k || !b_v))
+    return fail(HCR_ERR_INVALID_ARG, "has_kv_bias needs b_k and b_v");
+  if (!d.has_kv_bias && (b_k || b_v))
+    return fail(HCR_ERR_INVALID_ARG, "b_k/b_v given but has_kv_bias is 0");
+  for (int l = 0; l < d.n_layers; ++l) {
+    if (!gamma[l] || !w_k[l] || !w_v[l] || (ln && !beta[l]) ||
+        (d.has_kv_bias && (!b_k[l] || !b_v[l])))
+      return fail(HCR_ERR_INVALID_ARG, "layer %d: a parameter pointer is NULL", l);
+  }
+
+  auto* h = new (std::nothrow) hcr_handle();
+  if (!h) return fail(HCR_ERR_OOM, "host allocation of the handle failed");
+  Handle& H = h->impl;
+  H.dims = d;
+  const int32_t d_kv = d.n_kv_heads * d.head_dim;
+  const int64_t per_layer = int64_t(2) * d_kv * d.d_model;
+  cudaError_t e;
+  auto bail = [&](cudaError_t err, const char* what) {
+    hcr_status s = cuda_fail(err, what);
+    free_handle(H);
+    delete h;
+    return s;
+  };
+  if ((e = cudaGetDevice(&H.device)) != cudaSuccess) return bail(e, "cudaGetDevice");
+  if ((e = cudaDeviceGetAttribute(&H.num_sms, cudaDevAttrMultiProcessorCount, H.device)) !=
+      cudaSuccess)
+    return bail(e, "cudaDeviceGetAttribute");
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, H.device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, H.device);
+  if (major != 10 || minor != 3) {
+    free_handle(H);
+    delete h;
+    return fail(HCR_ERR_UNSUPPORTED, "device is sm_%d%d; this library is built for sm_103a",
+                major, minor);
+  }
+
+  if ((e = cudaMalloc(&H.w_packed, size_t(per_layer) * d.n_layers * 2)) != cudaSuccess)
+    return bail(e, "cudaMalloc(packed weights)");
+  if (ln && (e = cudaMalloc(&H.col_sum, sizeof(float) * 2 * d_kv * d.n_layers)) != cudaSuccess)
+    return bail(e, "cudaMalloc(column sums)");
+  if ((ln || d.has_kv_bias) &&
+      (e = cudaMalloc(&H.col_bias, sizeof(float) * 2 * d_kv * d.n_layers)) != cudaSuccess)
+    return bail(e, "cudaMalloc(column bias)");
+  if ((e = cudaMalloc(&H.err, sizeof(uint32_t))) != cudaSuccess) return bail(e, "cudaMalloc(err)");
+  if ((e = cudaMemset(H.err, 0, sizeof(uint32_t))) != cudaSuccess) return bail(e, "cudaMemset");
+
+  for (int l = 0; l < d.n_layers; ++l) {
+    void* dst = static_cast<uint8_t*>(H.w_packed) + size_t(per_layer) * 2 * l;
+    if ((e = launch_pack_weights(w_k[l], w_v[l], gamma[l], dst, d_kv, d.d_model, d.dtype, 0)) !=
+        cudaSuccess)
+      return bail(e, "pack launch");
+    if (H.col_sum || H.col_bias) {
+      if ((e = launch_column_constants(dst, w_k[l], w_v[l], ln ? beta[l] : nullptr,
+                                       d.has_kv_bias ? b_k[l] : nullptr,
+                                       d.has_kv_bias ? b_v[l] : nullptr,
+                                       H.col_sum ? H.col_sum + int64_t(l) * 2 * d_kv : nullptr,
+                                       H.col_bias ? H.col_bias + int64_t(l) * 2 * d_kv : nullptr,
+                                       d_kv, d.d_model, d.dtype, ln, d.has_kv_bias, 0)) !=
+          cudaSuccess)
+        return bail(e, "column-constant launch");
+    }
+  }
+
+  if (d.rope) {
+    // cos/sin of pos * theta^(-2i/dh), evaluated in double precision and
+    // rounded once to float.
+    const int half = d.head_dim / 2;
+    std::vector<float> tab(size_t(d.max_position) * half * 2);
+    std::vector<double> omega(half);
+    for (int i = 0; i < half; ++i)
+      omega[i] = std::pow(double(d.rope_theta), -2.0 * i / double(d.head_dim));
+    for (int64_t p = 0; p < d.max_position; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double ang = double(p) * omega[i];
+        tab[(size_t(p) * half + i) * 2 + 0] = float(std::cos(ang));
+        tab[(size_t(p) * half + i) * 2 + 1] = float(std::sin(ang));
+      }
+    if ((e = cudaMalloc(&H.rope_tab, tab.size() * sizeof(float))) != cudaSuccess)
+      return bail(e, "cudaMalloc(rope table)");
+    if ((e = cudaMemcpy(H.rope_tab, tab.data(), tab.size() * sizeof(float),
+                        cudaMemcpyHostToDevice)) != cudaSuccess)
+      return bail(e, "cudaMemcpy(rope table)");
+  }
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) return bail(e, "create synchronize");
+
+  st = encode_3d(&H.tmap_w, H.w_packed, d.dtype, uint64_t(d.d_model), uint64_t(2) * d_kv,
+                 uint64_t(d.n_layers), kBlockN, "packed weights");
+  if (st != HCR_OK) {
+    free_handle(H);
+    delete h;
+    return st;
+  }
+  *out = h;
+  return HCR_OK;
+}
+
+void hcr_destroy(hcr_handle* h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  free_handle(h->impl);
+  delete h;
+}
+
+size_t hcr_workspace_bytes(const hcr_handle* h, int32_t n_tokens, int32_t n_layers_in_range) {
+  if (!h || n_tokens <= 0 || n_layers_in_range <= 0) return 0;
+  return workspace_layout(n_tokens, n_layers_in_range, h->impl.dims.norm == HCR_NORM_LAYER).total;
+}
+
+#define HCR_RESTORE_ARGS                                                                         \
+  RestoreArgs a{hidden,     layer_begin, layer_end,          n_req,   n_tokens,                  \
+                cu_seqlens, start_pos,   block_table,        max_blocks_per_req,                 \
+                k_cache,    v_cache,     layout,             workspace, workspace_bytes,         \
+                static_cast<cudaStream_t>(stream)}
+
+hcr_status hcr_restore_prepare(hcr_handle* h, const void* hidden, int32_t layer_begin,
+                               int32_t layer_end, int32_t n_req, int32_t n_tokens,
+                               const int32_t* cu_seqlens, const int32_t* start_pos,
+                               const int32_t* block_table, int32_t max_blocks_per_req,
+                               void* k_cache, void* v_cache, const hcr_cache_layout* layout,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  HCR_RESTORE_ARGS;
+  bool empty = false;
+  hcr_status st = validate_restore(h, a, &empty);
+  if (st != HCR_OK || empty) return st;
+  return do_prepare(h, a);
+}
+
+hcr_status hcr_restore_project(hcr_handle* h, const void* hidden, int32_t layer_begin,
+                               int32_t layer_end, int32_t n_req, int32_t n_tokens,
+                               const int32_t* cu_seqlens, const int32_t* start_pos,
+                               const int32_t* block_table, int32_t max_blocks_per_req,
+                               void* k_cache, void* v_cache, const hcr_cache_layout* layout,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  HCR_RESTORE_ARGS;
+  bool empty = false;
+  hcr_status st = validate_restore(h, a, &empty);
+  if (st != HCR_OK || empty) return st;
+  return do_project(h, a);
+}
+
+hcr_status hcr_restore(hcr_handle* h, const void* hidden, int32_t layer_begin, int32_t layer_end,
+                       int32_t n_req, int32_t n_tokens, const int32_t* cu_seqlens,
+                       const int32_t* start_pos, const int32_t* block_table,
+                       int32_t max_blocks_per_req, void* k_cache, void* v_cache,
+                       const hcr_cache_layout* layout, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  HCR_RESTORE_ARGS;
+  bool empty = false;
+  hcr_status st = validate_restore(h, a, &empty);
+  if (st != HCR_OK || empty) return st;
+  st = do_prepare(h, a);
+  if (st != HCR_OK) return st;
+  return do_project(h, a);
+}
+
+hcr_status hcr_check_device_error(hcr_handle* h, void* stream, uint32_t* flags) {
+  if (flags) *flags = 0;
+  if (!h) return fail(HCR_ERR_INVALID_ARG, "handle is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  uint32_t bits = 0;
+  if ((e = cudaMemcpyAsync(&bits, h->impl.err, sizeof bits, cudaMemcpyDeviceToHost, s)) !=
+      cudaSuccess)
+    return cuda_fail(e, "read device error word");
+  if ((e = cudaMemsetAsync(h->impl.err, 0, sizeof(uint32_t), s)) != cudaSuccess)
+    return cuda_fail(e, "clear device error word");
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  if (flags) *flags = bits;
+  if (bits & HCR_DEVERR_TIMEOUT) return fail(HCR_ERR_TIMEOUT, "device error bits 0x%x", bits);
+  if (bits) return fail(HCR_ERR_DEVICE_BOUNDS, "device error bits 0x%x", bits);
+  return HCR_OK;
+}
+
+int32_t hcr_num_sms(const hcr_handle* h) { return h ? h->impl.num_sms : 0; }
+
+}  // extern "C"

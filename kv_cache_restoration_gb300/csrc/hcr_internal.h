@@ -1,0 +1,138 @@
+// Internal declarations shared by the host API (hcr_api.cu) and the kernels
+// (hcr_prepare.cu, hcr_project.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/hcr.h"
+
+namespace hcr {
+
+// ---------------------------------------------------------------------------
+// Tiling of the fused K||V projection
+// ---------------------------------------------------------------------------
+constexpr int kBlockM = 128;           // tokens per tile (TMEM lanes)
+constexpr int kBlockN = 256;           // K||V columns per tile (TMEM columns per accumulator)
+constexpr int kBlockK = 64;            // 64 x 2 bytes = one 128-byte swizzle row
+constexpr int kUmmaK = 16;             // K of one tcgen05.mma kind::f16
+constexpr int kStages = 4;             // TMA -> MMA shared-memory ring depth
+constexpr int kAccums = 2;             // TMEM accumulators (epilogue overlaps next mainloop)
+constexpr int kTileBytesA = kBlockM * kBlockK * 2;
+constexpr int kTileBytesB = kBlockN * kBlockK * 2;
+constexpr int kStageBytes = kTileBytesA + kTileBytesB;
+constexpr int kProjectThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kEpilogueWarps = 4;
+constexpr int kGroupM = 16;            // m-tiles per raster group (L2 reuse of hidden rows)
+constexpr size_t kProjectSmemBytes = size_t(kStages) * kStageBytes + 1024;  // + align slack
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded pipeline waits: 2 s
+
+// tcgen05 instruction descriptor for kind::f16, fp32 accumulate, both
+// operands K-major: D format F32 (1) in bits [4,6), A and B format in
+// [7,10) and [10,13) (F16 = 0, BF16 = 1), N >> 3 in [17,23), M >> 4 in [24,29).
+constexpr uint32_t make_idesc_f16(int dtype, int m, int n) {
+  return (1u << 4) | (uint32_t(dtype == HCR_DTYPE_BF16 ? 1 : 0) << 7) |
+         (uint32_t(dtype == HCR_DTYPE_BF16 ? 1 : 0) << 10) | (uint32_t(n >> 3) << 17) |
+         (uint32_t(m >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------
+// Handle
+// ---------------------------------------------------------------------------
+struct Handle {
+  hcr_model_dims dims;
+  int device = 0;
+  int num_sms = 0;
+  void* w_packed = nullptr;    // [L][2*d_kv][d] storage dtype, gamma folded in
+  float* col_sum = nullptr;    // [L][2*d_kv] sum_i W'[j][i] (LayerNorm only)
+  float* col_bias = nullptr;   // [L][2*d_kv] folded bias (LN: W beta + b; RMS: b), or null
+  float2* rope_tab = nullptr;  // [max_position][head_dim/2] (cos, sin), or null
+  uint32_t* err = nullptr;     // device error word (HCR_DEVERR_* bits)
+  CUtensorMap tmap_w;          // 3-D map over w_packed: (d, 2*d_kv, L), box (64, 256, 1)
+  uint32_t debug_stall = 0;    // test hook: see hcr_debug_withhold_first_load
+};
+
+// ---------------------------------------------------------------------------
+// Workspace layout (all offsets 256-byte aligned)
+// ---------------------------------------------------------------------------
+struct WorkspaceLayout {
+  size_t slot_off, pos_off, rstd_off, mean_off, total;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WorkspaceLayout workspace_layout(int64_t n_tokens, int64_t n_layers, bool layer_norm) {
+  WorkspaceLayout w{};
+  size_t off = 0;
+  w.slot_off = off;
+  off = align_up(off + size_t(n_tokens) * 8, 256);
+  w.pos_off = off;
+  off = align_up(off + size_t(n_tokens) * 4, 256);
+  w.rstd_off = off;
+  off = align_up(off + size_t(n_tokens) * size_t(n_layers) * 4, 256);
+  w.mean_off = off;
+  if (layer_norm) off = align_up(off + size_t(n_tokens) * size_t(n_layers) * 4, 256);
+  w.total = off;
+  return w;
+}
+
+// ---------------------------------------------------------------------------
+// Kernel parameters
+// ---------------------------------------------------------------------------
+struct PrepareParams {
+  // A0: placement
+  const int32_t* cu_seqlens;
+  const int32_t* start_pos;
+  const int32_t* block_table;
+  int32_t n_req, n_tokens, max_blocks, num_blocks, block_size, max_position, check_position;
+  int64_t* slot;   // [T]; -1 marks a row that must not be written
+  int32_t* pos;    // [T]
+  // A1: norm statistics of rows (layer, token)
+  const void* hidden;  // [Lr][T][d]
+  int32_t n_layers, d_model, layer_norm, dtype;
+  float eps;
+  float* rstd;   // [Lr][T]
+  float* mean;   // [Lr][T] (LayerNorm only)
+  uint32_t* err;
+  int32_t slot_blocks;  // leading blocks of the grid that do placement
+};
+
+struct ProjectParams {
+  int32_t n_tokens, d_model, n_cols, d_kv, head_dim, n_layers, layer_begin;
+  int32_t m_tiles, n_tiles, k_blocks;
+  int64_t num_tiles;
+  int32_t layer_norm, has_bias, rope, dtype;
+  const int64_t* slot;
+  const int32_t* pos;
+  const float* rstd;
+  const float* mean;
+  const float* col_sum;   // base of layer layer_begin
+  const float* col_bias;  // base of layer layer_begin
+  const float2* rope_tab;
+  void* k_cache;          // base of layer layer_begin
+  void* v_cache;
+  int64_t layer_stride;   // elements
+  int32_t row_elems;      // n_kv_heads * head_dim
+  uint32_t* err;
+  uint32_t debug_stall;
+};
+
+// Launchers (return cudaGetLastError() of the launch).
+cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t s);
+cudaError_t launch_project(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
+                           const ProjectParams& p, int grid, cudaStream_t s);
+cudaError_t launch_pack_weights(const void* w_k, const void* w_v, const void* gamma, void* dst,
+                                int d_kv, int d, int dtype, cudaStream_t s);
+cudaError_t launch_column_constants(const void* w_packed, const void* w_k, const void* w_v,
+                                    const void* beta, const void* b_k, const void* b_v,
+                                    float* col_sum, float* col_bias, int d_kv, int d, int dtype,
+                                    int layer_norm, int has_bias, cudaStream_t s);
+
+}  // namespace hcr
+
+struct hcr_handle {
+  hcr::Handle impl;
+};

@@ -1,0 +1,370 @@
+// The fused K||V projection of a restore (HCache episode, "Fast State
+// Restoration for Evicted LLM KV Caches", cue 14: K = W_k H, V = W_v H).
+//
+// One persistent kernel per restore call covers every (layer, m-tile,
+// n-tile) of
+//     acc[t][j] = sum_i H_l[t][i] * W'_l[j][i],   W'_l = [W_k; W_v] diag(gamma)
+// on the 5th-generation tensor cores, and finishes each tile in registers:
+//     RMS:  x = rstd_t * acc                        (+ b_j if the model has K/V bias)
+//     LN:   x = rstd_t * (acc - mean_t * colsum_j) + (W beta + b)_j
+//     K columns: rotate-half RoPE at the token's absolute position
+//     cast to bf16/fp16 (round to nearest even) and 16-byte stores straight
+//     into the paged cache slot of the token; no intermediate K/V tensor.
+//
+// Ragged multi-request batches (cue 20: project all tokens of a layer
+// together so the GEMM shape stays regular) are handled by concatenating
+// every request's tokens along M: tiles are full except the very last one,
+// whatever the request lengths.
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0      one lane issues TMA loads of hidden and weight tiles into a
+//               kStages-deep shared-memory ring;
+//   warp 1      allocates TMEM (2 accumulators x 256 fp32 columns) and one
+//               lane issues tcgen05.mma (M=128, N=256, K=16) for each stage;
+//   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (each warp
+//               owns one 32-lane TMEM quadrant = 32 tokens), overlapping the
+//               MMA of the next tile into the other accumulator.
+// Every pipeline wait is bounded (kWaitLimitNs); on expiry the kernel sets
+// HCR_DEVERR_TIMEOUT, stops all roles, drains in-flight copies and MMAs with
+// a bounded wait, frees TMEM and returns.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "hcr_internal.h"
+#include "ptx.cuh"
+
+namespace hcr {
+namespace {
+
+struct TileCoord {
+  int l, m, n;
+};
+
+// Tile order: layer-major; inside a layer, groups of kGroupM m-tiles sweep
+// all n-tiles with m fastest, so the concurrently running CTAs share a few
+// weight tiles and a bounded set of hidden rows in L2.
+__device__ __forceinline__ TileCoord tile_coord(int64_t tile, const ProjectParams& p) {
+  const int64_t per_layer = int64_t(p.m_tiles) * p.n_tiles;
+  TileCoord c;
+  c.l = int(tile / per_layer);
+  const int r = int(tile - int64_t(c.l) * per_layer);
+  const int group_tiles = kGroupM * p.n_tiles;
+  const int g = r / group_tiles;
+  const int within = r - g * group_tiles;
+  const int rows = min(kGroupM, p.m_tiles - g * kGroupM);
+  c.m = g * kGroupM + within % rows;
+  c.n = within / rows;
+  return c;
+}
+
+struct __align__(8) PipeState {
+  uint64_t full[kStages];    // TMA -> MMA: stage filled
+  uint64_t empty[kStages];   // MMA -> TMA: stage consumed
+  uint64_t tfull[kAccums];   // MMA -> epilogue: accumulator complete
+  uint64_t tempty[kAccums];  // epilogue -> MMA: accumulator drained
+  uint64_t drain;            // MMA completion on shutdown
+  uint32_t tmem_base;
+  int32_t abort;
+};
+
+// Waits for the phase of `bar` with the given parity.  Gives up when another
+// role raised the abort flag or after kWaitLimitNs, raising it itself.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int32_t* abort,
+                                           uint32_t* err) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      atomicOr(err, uint32_t(HCR_DEVERR_TIMEOUT));
+      return false;
+    }
+  }
+}
+
+// Bounded wait used only while shutting down after an abort.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs / 4) return;
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (DT == HCR_DTYPE_BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void store16(uint16_t* dst, const float (&x)[16]) {
+  uint4 lo, hi;
+  lo.x = pack2<DT>(x[0], x[1]);
+  lo.y = pack2<DT>(x[2], x[3]);
+  lo.z = pack2<DT>(x[4], x[5]);
+  lo.w = pack2<DT>(x[6], x[7]);
+  hi.x = pack2<DT>(x[8], x[9]);
+  hi.y = pack2<DT>(x[10], x[11]);
+  hi.z = pack2<DT>(x[12], x[13]);
+  hi.w = pack2<DT>(x[14], x[15]);
+  reinterpret_cast<uint4*>(dst)[0] = lo;
+  reinterpret_cast<uint4*>(dst)[1] = hi;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kProjectThreads, 1)
+    project_kernel(const __grid_constant__ CUtensorMap tmap_h,
+                   const __grid_constant__ CUtensorMap tmap_w, const ProjectParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ PipeState ps;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem_a = smem;                                   // kStages x [128][64]
+  uint8_t* smem_b = smem + size_t(kStages) * kTileBytesA;   // kStages x [256][64]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int32_t* abort = &ps.abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&ps.full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&ps.empty[s]), 1);
+    }
+    for (int a = 0; a < kAccums; ++a) {
+      ptx::mbar_init(ptx::smem_u32(&ps.tfull[a]), 1);
+      ptx::mbar_init(ptx::smem_u32(&ps.tempty[a]), kEpilogueWarps);
+    }
+    ptx::mbar_init(ptx::smem_u32(&ps.drain), 1);
+    ps.abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(&ps.tmem_base), kAccums * kBlockN);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = ps.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmap_h);
+      ptx::tma_prefetch_desc(&tmap_w);
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const TileCoord c = tile_coord(tile, p);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_phase(ptx::smem_u32(&ps.empty[stage]), phase ^ 1u, abort, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = ptx::smem_u32(&ps.full[stage]);
+          ptx::mbar_arrive_expect_tx(full, kStageBytes);
+          if (!(p.debug_stall && issued == 0)) {
+            ptx::tma_load_3d(ptx::smem_u32(smem_a + size_t(stage) * kTileBytesA), &tmap_h, full,
+                             kb * kBlockK, c.m * kBlockM, c.l);
+            ptx::tma_load_3d(ptx::smem_u32(smem_b + size_t(stage) * kTileBytesB), &tmap_w, full,
+                             kb * kBlockK, c.n * kBlockN, p.layer_begin + c.l);
+          }
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Loads issued but possibly not consumed are among the last kStages.
+        const int64_t first = issued > kStages ? issued - kStages : 0;
+        for (int64_t i = first; i < issued; ++i)
+          drain_wait(ptx::smem_u32(&ps.full[i % kStages]), uint32_t((i / kStages) & 1));
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc_f16(DT, kBlockM, kBlockN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        if (!wait_phase(ptx::smem_u32(&ps.tempty[acc]), acc_phase ^ 1u, abort, p.err)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * kBlockN);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_phase(ptx::smem_u32(&ps.full[stage]), phase, abort, p.err)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a0 = ptx::smem_u32(smem_a + size_t(stage) * kTileBytesA);
+          const uint32_t b0 = ptx::smem_u32(smem_b + size_t(stage) * kTileBytesB);
+#pragma unroll
+          for (int k = 0; k < kBlockK / kUmmaK; ++k) {
+            ptx::mma_f16(d_tmem, ptx::sw128_kmajor_desc(a0 + k * kUmmaK * 2),
+                         ptx::sw128_kmajor_desc(b0 + k * kUmmaK * 2), idesc,
+                         (kb | k) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_u32(&ps.empty[stage]));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(ptx::smem_u32(&ps.tfull[acc]));
+        if (++acc == kAccums) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // Every MMA this thread issued has completed once `drain` flips.
+      ptx::mma_commit(ptx::smem_u32(&ps.drain));
+      drain_wait(ptx::smem_u32(&ps.drain), 0);
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int quad = warp & 3;               // TMEM lanes [32*quad, 32*quad+32)
+    const int row = quad * 32 + lane;        // token row within the tile
+    const int half = p.head_dim >> 1;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+      const TileCoord c = tile_coord(tile, p);
+      int ok = 0;
+      if (lane == 0) ok = wait_phase(ptx::smem_u32(&ps.tfull[acc]), acc_phase, abort, p.err);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ptx::tc_fence_after();
+
+      const int t = c.m * kBlockM + row;
+      bool valid = t < p.n_tokens;
+      int64_t slot = -1;
+      int pos = 0;
+      float rstd = 0.f, mean = 0.f;
+      if (valid) {
+        slot = __ldg(p.slot + t);
+        pos = __ldg(p.pos + t);
+        const int64_t srow = int64_t(c.l) * p.n_tokens + t;
+        rstd = __ldg(p.rstd + srow);
+        if (p.layer_norm) mean = __ldg(p.mean + srow);
+      }
+      valid = valid && slot >= 0;
+      const float* csum = p.layer_norm ? p.col_sum + int64_t(c.l) * p.n_cols : nullptr;
+      const float* cbias = p.has_bias ? p.col_bias + int64_t(c.l) * p.n_cols : nullptr;
+      const uint32_t tacc = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * kBlockN);
+
+      for (int h0 = 0; h0 < kBlockN; h0 += p.head_dim) {
+        const int col0 = c.n * kBlockN + h0;
+        if (col0 >= p.n_cols) break;   // ragged last n-tile (warp-uniform)
+        const bool is_k = col0 < p.d_kv;
+        const int head = (is_k ? col0 : col0 - p.d_kv) / p.head_dim;
+        uint16_t* dst = nullptr;
+        if (valid) {
+          uint16_t* base = reinterpret_cast<uint16_t*>(is_k ? p.k_cache : p.v_cache);
+          dst = base + int64_t(c.l) * p.layer_stride + slot * int64_t(p.row_elems) +
+                int64_t(head) * p.head_dim;
+        }
+        const bool do_rope = is_k && p.rope;
+        for (int j = 0; j < half; j += 16) {
+          uint32_t ra[16], rb[16];
+          ptx::tmem_ld16(tacc + uint32_t(h0 + j), ra);
+          ptx::tmem_ld16(tacc + uint32_t(h0 + half + j), rb);
+          ptx::tmem_ld_wait();
+          float a[16], b[16];
+          const int ca = col0 + j, cb = col0 + half + j;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float xa = __uint_as_float(ra[i]);
+            float xb = __uint_as_float(rb[i]);
+            if (p.layer_norm) {
+              xa = rstd * (xa - mean * __ldg(csum + ca + i));
+              xb = rstd * (xb - mean * __ldg(csum + cb + i));
+            } else {
+              xa *= rstd;
+              xb *= rstd;
+            }
+            if (cbias) {
+              xa += __ldg(cbias + ca + i);
+              xb += __ldg(cbias + cb + i);
+            }
+            a[i] = xa;
+            b[i] = xb;
+          }
+          if (do_rope && valid) {
+            const float4* tab =
+                reinterpret_cast<const float4*>(p.rope_tab + int64_t(pos) * half + j);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 cs = __ldg(tab + i);   // (cos, sin) of pairs j+2i, j+2i+1
+              const float a0 = a[2 * i], b0 = b[2 * i];
+              const float a1 = a[2 * i + 1], b1 = b[2 * i + 1];
+              a[2 * i] = a0 * cs.x - b0 * cs.y;
+              b[2 * i] = b0 * cs.x + a0 * cs.y;
+              a[2 * i + 1] = a1 * cs.z - b1 * cs.w;
+              b[2 * i + 1] = b1 * cs.z + a1 * cs.w;
+            }
+          }
+          if (valid) {
+            store16<DT>(dst + j, a);
+            store16<DT>(dst + half + j, b);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ps.tempty[acc]));
+      if (++acc == kAccums) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kAccums * kBlockN);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_project(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
+                           const ProjectParams& p, int grid, cudaStream_t s) {
+  if (p.dtype == HCR_DTYPE_BF16) {
+    cudaError_t e = cudaFuncSetAttribute(project_kernel<HCR_DTYPE_BF16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kProjectSmemBytes));
+    if (e != cudaSuccess) return e;
+    project_kernel<HCR_DTYPE_BF16><<<grid, kProjectThreads, kProjectSmemBytes, s>>>(tmap_h, tmap_w,
+                                                                                  p);
+  } else {
+    cudaError_t e = cudaFuncSetAttribute(project_kernel<HCR_DTYPE_FP16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kProjectSmemBytes));
+    if (e != cudaSuccess) return e;
+    project_kernel<HCR_DTYPE_FP16><<<grid, kProjectThreads, kProjectSmemBytes, s>>>(tmap_h, tmap_w,
+                                                                                  p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace hcr

@@ -1,0 +1,90 @@
+"""The C ABI without a GPU: the library builds and loads, exports every symbol
+include/hcr.h declares, and rejects bad create arguments on the host before
+any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def B():
+    from kv_cache_restoration_gb300 import build
+    build.build()
+    from kv_cache_restoration_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "hcr.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hcr_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("hcr_create", "hcr_restore", "hcr_destroy", "hcr_workspace_bytes",
+              "hcr_check_device_error", "hcr_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(B):
+    lib = ctypes.CDLL(B.LIB)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(B):
+    for s in range(8):
+        assert B.hcr_status_string(s).startswith("HCR_")
+    assert "unknown" in B.hcr_status_string(99)
+
+
+def _dims(B, **kw):
+    from kv_cache_restoration_gb300 import make_dims
+    d = make_dims(2, 256, 4, 4, 64, max_position=128)
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+FAKE = [0x1000, 0x2000]   # never dereferenced: every case below fails validation first
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("n_layers", 0, 1), ("d_model", 100, 1), ("d_model", 0, 1), ("n_kv_heads", 0, 1),
+    ("n_heads", 6, 1), ("head_dim", 96, 2), ("norm", 5, 1), ("norm_eps", -1.0, 1),
+    ("rope", 3, 1), ("rope_theta", 0.0, 1), ("max_position", 0, 1), ("dtype", 7, 1),
+])
+def test_create_rejects_bad_dims(B, field, value, status):
+    st, h = B.hcr_create(_dims(B, **{field: value}), FAKE, None, FAKE, FAKE, check=False)
+    assert st == status and h is None
+    assert B.hcr_last_error()
+
+
+def test_create_rejects_bad_pointers(B):
+    d = _dims(B)
+    assert B.hcr_create(d, None, None, FAKE, FAKE, check=False)[0] == B.HCR_ERR_INVALID_ARG
+    assert B.hcr_create(d, FAKE, FAKE, FAKE, FAKE, check=False)[0] == B.HCR_ERR_INVALID_ARG
+    assert B.hcr_create(d, [0x1000, 0], None, FAKE, FAKE, check=False)[0] == \
+        B.HCR_ERR_INVALID_ARG
+    assert B.hcr_create(d, FAKE, None, FAKE, FAKE, FAKE, FAKE, check=False)[0] == \
+        B.HCR_ERR_INVALID_ARG
+    ln = _dims(B, norm=B.HCR_NORM_LAYER)
+    assert B.hcr_create(ln, FAKE, None, FAKE, FAKE, check=False)[0] == B.HCR_ERR_INVALID_ARG
+    bias = _dims(B, has_kv_bias=1)
+    assert B.hcr_create(bias, FAKE, None, FAKE, FAKE, check=False)[0] == B.HCR_ERR_INVALID_ARG
+
+
+def test_null_handle_calls(B):
+    assert B.hcr_workspace_bytes(None, 10, 1) == 0
+    assert B.hcr_num_sms(None) == 0
+    B.hcr_destroy(None)
+    st = B.hcr_restore(None, None, 0, 1, 1, 1, None, None, None, 1, None, None, None, None, 0,
+                       check=False)
+    assert st == B.HCR_ERR_INVALID_ARG
+    assert B.hcr_check_device_error(None)[0] == B.HCR_ERR_INVALID_ARG

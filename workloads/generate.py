@@ -163,3 +163,52 @@ def sentinel_cache(n_layers: int, num_blocks: int, block_size: int, n_kv_heads: 
                     dtype=torch.int16, device=device)
     t.fill_(SENTINEL_BITS)
     return t.view(TORCH_DTYPE[dtype])
+
+
+@dataclass
+class DeviceInputs:
+    """Everything one restore call reads or writes, resident on a device."""
+    params: list                 # LayerParams per model layer
+    layout: RequestLayout
+    hidden: torch.Tensor         # [Lr][T][d] for layers [layer_begin, layer_end)
+    k_cache: torch.Tensor        # [Lr][num_blocks][B][H_kv][dh], sentinel-filled
+    v_cache: torch.Tensor
+    cu: torch.Tensor             # int32 [R+1]
+    start: torch.Tensor          # int32 [R]
+    table: torch.Tensor          # int32 [R][max_blocks]
+
+
+def device_inputs(w: Workload, device, layer_begin: int = 0, layer_end: Optional[int] = None,
+                  params: Optional[list] = None, gen_device=None) -> DeviceInputs:
+    """Seeded inputs for layers [layer_begin, layer_end) of workload w on `device`.
+
+    Random tensors are drawn on gen_device (default: the CPU for small
+    workloads, `device` for large ones) and copied; hidden layer i is drawn
+    from the stream of absolute layer layer_begin + i, so splitting a layer
+    range gives the same inputs.
+    """
+    s = w.shape
+    layer_end = s.n_layers if layer_end is None else layer_end
+    if gen_device is None:
+        big = w.n_tokens * s.d_model * (layer_end - layer_begin) > (1 << 26)
+        gen_device = device if big else "cpu"
+    if params is None:
+        params = []
+        for l in range(s.n_layers):
+            p = layer_params(s, l, w.seed, gen_device)
+            params.append(LayerParams(*[None if t is None else t.to(device) for t in
+                                        (p.gamma, p.beta, p.w_k, p.w_v, p.b_k, p.b_v)]))
+    lay = request_layout(w)
+    Lr = layer_end - layer_begin
+    hidden = torch.empty((Lr, w.n_tokens, s.d_model), dtype=TORCH_DTYPE[s.dtype], device=device)
+    for i in range(Lr):
+        hidden[i].copy_(hidden_states(w, layer_begin + i, gen_device))
+    kc = sentinel_cache(Lr, lay.num_blocks, w.block_size, s.n_kv_heads, s.head_dim, s.dtype,
+                        device)
+    vc = sentinel_cache(Lr, lay.num_blocks, w.block_size, s.n_kv_heads, s.head_dim, s.dtype,
+                        device)
+
+    def to(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return DeviceInputs(params, lay, hidden, kc, vc, to(lay.cu_seqlens), to(lay.start_pos),
+                        to(lay.block_table))

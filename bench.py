@@ -170,12 +170,12 @@ def gpu_arm(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
 
-    from kv_cache_restoration_gb300 import build as build_mod
     from workloads import configs as C
     from workloads import generate as G
 
     if rank == 0:
-        build_mod.build()
+        import __graft_entry__
+        __graft_entry__._build_module().build()
     if world > 1:
         dist.barrier()
     from kv_cache_restoration_gb300 import Restorer, make_dims

@@ -8,6 +8,17 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def pytest_sessionstart(session):
+    # Build libhcr.so in-tree if it is missing or stale (nvcc cross-compiles
+    # without a GPU), so the binding can load it.
+    import importlib.util
+    path = os.path.join(ROOT, "kv_cache_restoration_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("hcr_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running GPU case at full workload size")

@@ -12,9 +12,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def B():
-    from kv_cache_restoration_gb300 import build
-    build.build()
-    from kv_cache_restoration_gb300 import binding
+    from kv_cache_restoration_gb300 import binding   # built at session start
     return binding
 
 

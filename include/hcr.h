@@ -193,6 +193,41 @@ hcr_status hcr_restore_project(hcr_handle* h, const void* hidden, int32_t layer_
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * hcr_restore_no_alloc -- hcr_restore without a caller-provided workspace.
+ *
+ * The paper has no counterpart to this call; it exists for callers of this
+ * library that cannot allocate device memory when they need a restore, for
+ * example a serving engine that gave all free HBM to its paged KV pool at
+ * start-up, or one that must not call cudaMalloc/cudaFree (which can
+ * synchronise the device) while decode kernels run on its other streams.
+ *
+ * Same arguments and results as hcr_restore, minus workspace and
+ * workspace_bytes.  The scratch is one fixed array of
+ * HCR_NO_ALLOC_SCRATCH_BYTES in device global memory, part of the library
+ * image: every GPU that loads the library holds it until the process exits.
+ * A restore whose hcr_workspace_bytes() exceeds that size is rejected with
+ * HCR_ERR_WORKSPACE before anything is enqueued (restore fewer tokens or
+ * layers per call).  The handle's device must be current.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call on a device shares the one array,
+ * which keeps the last call's contents; nothing in it needs to start at
+ * zero (each restore writes every scratch word it later reads).  Calls
+ * whose GPU work can overlap -- on different streams, or from different
+ * handles, without ordering between them -- race on the array and give
+ * undefined results.  This call allocates nothing: no cudaMalloc, cudaFree
+ * or allocating library routine.
+ */
+#define HCR_NO_ALLOC_SCRATCH_BYTES (16u << 20)
+hcr_status hcr_restore_no_alloc(hcr_handle* h, const void* hidden, int32_t layer_begin,
+                                int32_t layer_end, int32_t n_req, int32_t n_tokens,
+                                const int32_t* cu_seqlens, const int32_t* start_pos,
+                                const int32_t* block_table, int32_t max_blocks_per_req,
+                                void* k_cache, void* v_cache, const hcr_cache_layout* layout,
+                                void* stream);
+
+/*
  * hcr_check_device_error -- synchronise `stream`, then read and clear the
  * handle's device error word.  Returns HCR_OK, HCR_ERR_DEVICE_BOUNDS or
  * HCR_ERR_TIMEOUT (timeout wins), or HCR_ERR_CUDA if the synchronisation

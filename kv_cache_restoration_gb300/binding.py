@@ -78,6 +78,9 @@ lib.hcr_workspace_bytes.restype = ctypes.c_size_t
 for _name in ("hcr_restore", "hcr_restore_prepare", "hcr_restore_project"):
     getattr(lib, _name).argtypes = _RESTORE_ARGTYPES
     getattr(lib, _name).restype = ctypes.c_int
+lib.hcr_restore_no_alloc.argtypes = _RESTORE_ARGTYPES[:13] + [_vp]
+lib.hcr_restore_no_alloc.restype = ctypes.c_int
+HCR_NO_ALLOC_SCRATCH_BYTES = 16 << 20
 lib.hcr_check_device_error.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]
 lib.hcr_check_device_error.restype = ctypes.c_int
 lib.hcr_status_string.argtypes = [ctypes.c_int]
@@ -183,6 +186,20 @@ def hcr_restore_project(handle, hidden, layer_begin, layer_end, n_req, n_tokens,
                          layer_begin, layer_end, n_req, n_tokens, cu_seqlens, start_pos,
                          block_table, max_blocks_per_req, k_cache, v_cache, layout, workspace,
                          workspace_bytes, stream, check)
+
+
+def hcr_restore_no_alloc(handle, hidden, layer_begin, layer_end, n_req, n_tokens, cu_seqlens,
+                         start_pos, block_table, max_blocks_per_req, k_cache, v_cache, layout,
+                         stream=None, *, check: bool = True) -> int:
+    """hcr_restore with the library's built-in scratch array (no workspace argument)."""
+    st = lib.hcr_restore_no_alloc(handle, _ptr(hidden), layer_begin, layer_end, n_req, n_tokens,
+                                  _ptr(cu_seqlens), _ptr(start_pos), _ptr(block_table),
+                                  max_blocks_per_req, _ptr(k_cache), _ptr(v_cache),
+                                  ctypes.byref(layout) if layout is not None else None,
+                                  _stream_ptr(stream))
+    if check:
+        _check(st, "hcr_restore_no_alloc")
+    return st
 
 
 def hcr_check_device_error(handle, stream=None):

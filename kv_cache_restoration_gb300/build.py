@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhcr.so")
 
-SOURCES = ["hcr_api.cu", "hcr_prepare.cu", "hcr_project.cu"]
+SOURCES = ["hcr_api.cu", "hcr_prepare.cu", "hcr_project.cu", "hcr_no_alloc.cu"]
 HEADERS = ["hcr_internal.h", "ptx.cuh"]
 
 NVCC_FLAGS = [

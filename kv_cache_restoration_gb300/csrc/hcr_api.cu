@@ -256,6 +256,17 @@ void free_handle(Handle& H) {
 }
 
 }  // namespace
+
+hcr_status set_last_error(hcr_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
 }  // namespace hcr
 
 using namespace hcr;

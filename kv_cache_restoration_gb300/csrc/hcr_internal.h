@@ -120,6 +120,9 @@ struct ProjectParams {
   uint32_t debug_stall;
 };
 
+// Records a message for hcr_last_error() on this host thread; returns s.
+hcr_status set_last_error(hcr_status s, const char* fmt, ...);
+
 // Launchers (return cudaGetLastError() of the launch).
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t s);
 cudaError_t launch_project(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,

@@ -113,12 +113,26 @@ WORKLOADS = {
 }
 
 
+SHAPES = {s.name: s for s in (TINY, LLAMA2_7B, LLAMA2_13B, OPT_30B)}
+
+
 def get(name: str, **overrides) -> Workload:
+    """A named workload; "<shape>-T<n>" is one request of n tokens at position 0."""
     if name == "ragged-7b":
         w = ragged_7b()
-    else:
+    elif name in WORKLOADS:
         w = WORKLOADS[name]
+    elif "-T" in name and name.rsplit("-T", 1)[0] in SHAPES:
+        base, n = name.rsplit("-T", 1)
+        w = short_n(SHAPES[base], int(n))
+    else:
+        raise KeyError(name)
     return replace(w, **overrides) if overrides else w
+
+
+def with_layers(w: Workload, n_layers: int) -> Workload:
+    """The same workload on a model cut to its first n_layers layers."""
+    return replace(w, name=f"{w.name}-L{n_layers}", shape=replace(w.shape, n_layers=n_layers))
 
 
 def short_n(shape: ModelShape, n_tokens: int, seed: int = 0) -> Workload:

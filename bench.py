@@ -390,7 +390,7 @@ def main():
                        args.oracle_max_reps)
         cpu = {"value": o["value"], "unit": "tokens/s", "cores": o["cores"], "kind": "oracle",
                "sample": f"1 layer x {o['rows']} tokens of the {w.name} workload, "
-                         f"{o['reps']} reps (median), extrapolated to all {s.n_layers} layers"}
+                         f"{o['reps']} reps (mean), extrapolated to all {s.n_layers} layers"}
     line = {
         "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,

@@ -235,6 +235,21 @@ hcr_status hcr_restore_no_alloc(hcr_handle* h, const void* hidden, int32_t layer
  */
 hcr_status hcr_check_device_error(hcr_handle* h, void* stream, uint32_t* flags);
 
+/*
+ * hcr_debug_set_stall -- testing hook for the bounded pipeline waits.
+ *
+ * With enable != 0, later restores through this handle arm the first
+ * shared-memory stage of each CTA without issuing its loads, so the tensor
+ * core's wait for that stage can never complete.  The wait gives up after
+ * its time limit (2 s), the kernel sets HCR_DEVERR_TIMEOUT, stops every
+ * role, drains its in-flight copies and MMAs with bounded waits, frees its
+ * tensor memory and returns; hcr_check_device_error then reports
+ * HCR_ERR_TIMEOUT and the CUDA context stays usable.  enable = 0 restores
+ * normal operation.  Not for production use; do not change it while a
+ * restore through the handle may be enqueued.
+ */
+hcr_status hcr_debug_set_stall(hcr_handle* h, int32_t enable);
+
 /* Static description of a status code. */
 const char* hcr_status_string(hcr_status s);
 

@@ -89,6 +89,8 @@ lib.hcr_last_error.argtypes = []
 lib.hcr_last_error.restype = ctypes.c_char_p
 lib.hcr_num_sms.argtypes = [_vp]
 lib.hcr_num_sms.restype = _i32
+lib.hcr_debug_set_stall.argtypes = [_vp, _i32]
+lib.hcr_debug_set_stall.restype = ctypes.c_int
 
 
 def hcr_status_string(status: int) -> str:
@@ -211,3 +213,8 @@ def hcr_check_device_error(handle, stream=None):
 
 def hcr_num_sms(handle) -> int:
     return lib.hcr_num_sms(handle)
+
+
+def hcr_debug_set_stall(handle, enable: bool) -> int:
+    """Testing hook: make restores through `handle` run into the bounded-wait timeout."""
+    return lib.hcr_debug_set_stall(handle, 1 if enable else 0)

@@ -479,4 +479,10 @@ hcr_status hcr_check_device_error(hcr_handle* h, void* stream, uint32_t* flags) 
 
 int32_t hcr_num_sms(const hcr_handle* h) { return h ? h->impl.num_sms : 0; }
 
+hcr_status hcr_debug_set_stall(hcr_handle* h, int32_t enable) {
+  if (!h) return fail(HCR_ERR_INVALID_ARG, "handle is NULL");
+  h->impl.debug_stall = enable ? 1u : 0u;
+  return HCR_OK;
+}
+
 }  // extern "C"

@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = ps.tmem_base;
 
+  int64_t issued = 0;   // TMA stages armed by the producer (warp 0, lane 0)
   if (warp == 0) {
     // ------------------------------------------------------------- TMA producer
     if (lane == 0) {
@@ -163,7 +164,6 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
       ptx::tma_prefetch_desc(&tmap_w);
       int stage = 0;
       uint32_t phase = 0;
-      int64_t issued = 0;
       bool ok = true;
       for (int64_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
         const TileCoord c = tile_coord(tile, p);
@@ -186,12 +186,6 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
             phase ^= 1u;
           }
         }
-      }
-      if (!ok) {
-        // Loads issued but possibly not consumed are among the last kStages.
-        const int64_t first = issued > kStages ? issued - kStages : 0;
-        for (int64_t i = first; i < issued; ++i)
-          drain_wait(ptx::smem_u32(&ps.full[i % kStages]), uint32_t((i / kStages) & 1));
       }
     }
   } else if (warp == 1) {
@@ -339,6 +333,17 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
+  if (*abort) {
+    // Some role gave up: loads the producer armed may still be landing in
+    // shared memory.  They are among its last kStages; wait for each (bounded)
+    // before the CTA releases its memory.
+    if (warp == 0 && lane == 0) {
+      const int64_t first = issued > kStages ? issued - kStages : 0;
+      for (int64_t i = first; i < issued; ++i)
+        drain_wait(ptx::smem_u32(&ps.full[i % kStages]), uint32_t((i / kStages) & 1));
+    }
+    __syncthreads();
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kAccums * kBlockN);

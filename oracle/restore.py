@@ -44,16 +44,24 @@ import numpy as np
 def widen_bits(bits: np.ndarray, dtype: str) -> np.ndarray:
     """Exact float64 value of bf16 or IEEE binary16 bit patterns (uint16).
 
-    bf16 is the upper half of an IEEE binary32 word.  binary16 has 1 sign
-    bit, 5 exponent bits (bias 15) and 10 fraction bits; exponent 0 encodes
-    subnormals 2^-14 * f/1024, exponent 31 encodes inf/NaN.
+    bf16 is the upper half of an IEEE binary32 word; binary16 is numpy's
+    float16.  Both widen to float64 exactly.  fp16_from_fields decodes
+    binary16 from its fields and pins this conversion in the tests.
     """
     b = np.asarray(bits).astype(np.uint16)
-    if dtype == "bf16":
-        with np.errstate(invalid="ignore"):   # signalling-NaN patterns widen to NaN
+    with np.errstate(invalid="ignore"):   # signalling-NaN patterns widen to NaN
+        if dtype == "bf16":
             return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
-    if dtype != "fp16":
-        raise ValueError(dtype)
+        if dtype == "fp16":
+            return b.view(np.float16).astype(np.float64)
+    raise ValueError(dtype)
+
+
+def fp16_from_fields(bits: np.ndarray) -> np.ndarray:
+    """binary16 from its definition: 1 sign bit, 5 exponent bits (bias 15), 10
+    fraction bits; exponent 0 encodes subnormals 2^-14 * f/1024, exponent 31
+    encodes inf (f = 0) and NaN."""
+    b = np.asarray(bits).astype(np.uint16)
     sign = np.where((b >> 15) & 1, -1.0, 1.0)
     e = ((b >> 10) & 0x1F).astype(np.int64)
     f = (b & 0x3FF).astype(np.float64)

@@ -153,17 +153,29 @@ def compare(case: Case, rows: Optional[np.ndarray] = None,
 
 def check_sentinels(case: Case, written_slots: np.ndarray):
     """Every slot no restored token maps to keeps the sentinel, bit for bit, in
-    every layer of both caches (checked on the device, counted on the host)."""
-    s = case.w.shape
+    every layer of both caches, and every restored slot was written (checked
+    on the device one layer at a time, counted on the host)."""
     nslots = case.layout.num_blocks * case.layout.block_size
     mask = torch.ones(nslots, dtype=torch.bool, device=case.k_cache.device)
     if len(written_slots):
         mask[torch.as_tensor(written_slots, device=mask.device)] = False
     for c, name in ((case.k_cache, "K"), (case.v_cache, "V")):
-        bits = c.view(torch.int16).reshape(c.shape[0], nslots, -1)
-        untouched = bits[:, mask, :]
-        n_bad = int((untouched != G.SENTINEL_BITS).sum().item())
-        assert n_bad == 0, f"{name} cache: {n_bad} elements of unwritten slots changed"
-        written = bits[:, ~mask, :]
-        n_sent = int((written == G.SENTINEL_BITS).sum().item())
-        assert n_sent == 0, f"{name} cache: {n_sent} elements of restored slots not written"
+        for li in range(c.shape[0]):
+            bits = c[li].view(torch.int16).reshape(nslots, -1)
+            n_bad = int((bits[mask] != G.SENTINEL_BITS).sum().item())
+            assert n_bad == 0, f"{name} cache layer {li}: {n_bad} elements of unwritten slots changed"
+            n_sent = int((bits[~mask] == G.SENTINEL_BITS).sum().item())
+            assert n_sent == 0, f"{name} cache layer {li}: {n_sent} restored elements not written"
+
+
+def sample_rows(w: Workload, fraction: float, seed: int = 1) -> np.ndarray:
+    """A seeded sample of token rows plus every request's first and last row."""
+    T = w.n_tokens
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n = max(64, int(T * fraction))
+    rows = set(rng.choice(T, size=min(n, T), replace=False).tolist())
+    cu = np.concatenate([[0], np.cumsum(w.seq_lens)])
+    for r in range(w.n_req):
+        if cu[r + 1] > cu[r]:
+            rows.update((int(cu[r]), int(cu[r + 1] - 1)))
+    return np.array(sorted(rows), dtype=np.int64)

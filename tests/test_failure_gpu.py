@@ -1,0 +1,29 @@
+"""Failure detection on the GPU without faulting it: a pipeline wait that can
+never complete gives up after its time limit, the kernel reports
+HCR_ERR_TIMEOUT through the device error word, and the CUDA context stays
+usable for the next restore."""
+import time
+
+import pytest
+
+from tests import harness as Hn
+from workloads import configs as C
+
+pytestmark = pytest.mark.gpu
+
+
+def test_stalled_pipeline_times_out_and_context_survives(cuda_device):
+    from kv_cache_restoration_gb300 import binding as B
+    w = C.get("tiny")
+    case = Hn.make_case(w, cuda_device)
+    assert B.hcr_debug_set_stall(case.restorer.handle, True) == B.HCR_OK
+    t0 = time.monotonic()
+    Hn.run(case)
+    elapsed = time.monotonic() - t0
+    assert case.status == B.HCR_ERR_TIMEOUT
+    assert case.flags & B.HCR_DEVERR_TIMEOUT
+    assert 1.5 < elapsed < 60.0
+    assert B.hcr_debug_set_stall(case.restorer.handle, False) == B.HCR_OK
+    again = Hn.run(Hn.make_case(w, cuda_device, params=case.params, restorer=case.restorer))
+    assert again.status == 0
+    Hn.compare(again)

@@ -24,7 +24,12 @@ def test_widen_bf16_all_patterns():
 def test_widen_fp16_all_patterns():
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     got = R.widen_bits(bits, "fp16")
-    want = bits.view(np.float16).astype(np.float64)
+    want = R.fp16_from_fields(bits)          # decoded from the binary16 fields
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+    # and the field decoding agrees with torch's half conversion
+    want = torch.from_numpy(bits.view(np.int16)).view(torch.float16).to(torch.float64).numpy()
     assert np.array_equal(np.isnan(got), np.isnan(want))
     ok = ~np.isnan(want)
     assert np.array_equal(got[ok], want[ok])

@@ -214,6 +214,10 @@ def gpu_arm(args, rank, world, local_rank):
                            s.norm_eps, s.rope, s.rope_theta, w.rope_positions, s.dtype,
                            s.kv_bias), case.params)
     case.params = None           # the handle holds packed copies
+    if args.variant:
+        from kv_cache_restoration_gb300 import binding as B
+        if B.hcr_debug_set_variant(r.handle, args.variant) != 0:
+            raise RuntimeError(B.hcr_last_error())
     lay = case.layout
     L, T = s.n_layers, w.n_tokens
     ws = r.workspace(T, L, device)
@@ -294,6 +298,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="llama2-7b")
     ap.add_argument("--e2e-steps", type=int, default=30, help="0 skips the end-to-end leg")
+    ap.add_argument("--variant", type=int, default=0,
+                    help="project kernel tiles: 0 automatic, 1 single CTAs, 2 CTA pairs")
     ap.add_argument("--layers", type=int, default=0,
                     help="cut the model to its first N layers (small profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -397,6 +403,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": s.dtype, "data": "synthetic",
         "config": {"workload": workload_desc,
+                   "project_variant": {0: "auto", 1: "single", 2: "pair"}[args.variant],
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2 ({(hid_b + w_b + kv_b) / 1e9:.2f} GB "
                          "moved per step vs 129 MB L2); no flush"},

@@ -250,6 +250,17 @@ hcr_status hcr_check_device_error(hcr_handle* h, void* stream, uint32_t* flags);
  */
 hcr_status hcr_debug_set_stall(hcr_handle* h, int32_t enable);
 
+/*
+ * hcr_debug_set_variant -- testing hook: which project-kernel variant later
+ * restores through this handle use.  0 (default): automatic -- CTA pairs
+ * (cta_group::2, 256-token tiles) for restores of more than 128 tokens,
+ * single CTAs (128-token tiles) otherwise; 1: always single CTAs; 2: always
+ * CTA pairs (HCR_ERR_UNSUPPORTED if the device cannot co-schedule them).
+ * Both variants compute the same values bit for bit.  Do not change it while
+ * a restore through the handle may be enqueued.
+ */
+hcr_status hcr_debug_set_variant(hcr_handle* h, int32_t variant);
+
 /* Static description of a status code. */
 const char* hcr_status_string(hcr_status s);
 

@@ -89,6 +89,8 @@ lib.hcr_last_error.argtypes = []
 lib.hcr_last_error.restype = ctypes.c_char_p
 lib.hcr_num_sms.argtypes = [_vp]
 lib.hcr_num_sms.restype = _i32
+lib.hcr_debug_set_variant.argtypes = [_vp, _i32]
+lib.hcr_debug_set_variant.restype = ctypes.c_int
 lib.hcr_debug_set_stall.argtypes = [_vp, _i32]
 lib.hcr_debug_set_stall.restype = ctypes.c_int
 
@@ -213,6 +215,11 @@ def hcr_check_device_error(handle, stream=None):
 
 def hcr_num_sms(handle) -> int:
     return lib.hcr_num_sms(handle)
+
+
+def hcr_debug_set_variant(handle, variant: int) -> int:
+    """Testing hook: 0 automatic, 1 single-CTA tiles, 2 CTA-pair tiles."""
+    return lib.hcr_debug_set_variant(handle, variant)
 
 
 def hcr_debug_set_stall(handle, enable: bool) -> int:

@@ -213,7 +213,14 @@ hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
   p.head_dim = d.head_dim;
   p.n_layers = nl;
   p.layer_begin = a.layer_begin;
-  p.m_tiles = (a.n_tokens + kBlockM - 1) / kBlockM;
+  // CTA pairs (256-row tiles) once there is more than one 128-row tile of
+  // tokens; single CTAs for short restores, which stream weights from HBM
+  // and would only pad the pair's second half.
+  bool pair = H.pair_clusters > 0 && a.n_tokens > kBlockM;
+  if (H.variant == 1) pair = false;
+  if (H.variant == 2) pair = H.pair_clusters > 0;
+  const int tile_m = pair ? 2 * kBlockM : kBlockM;
+  p.m_tiles = (a.n_tokens + tile_m - 1) / tile_m;
   p.n_tiles = (2 * d_kv + kBlockN - 1) / kBlockN;
   p.k_blocks = (d.d_model + kBlockK - 1) / kBlockK;
   p.num_tiles = int64_t(nl) * p.m_tiles * p.n_tiles;
@@ -237,8 +244,10 @@ hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
   p.row_elems = d_kv;
   p.err = H.err;
   p.debug_stall = H.debug_stall;
-  const int grid = int(std::min<int64_t>(p.num_tiles, H.num_sms));
-  cudaError_t e = launch_project(tmap_h, H.tmap_w, p, grid, a.stream);
+  const int grid = pair ? 2 * int(std::min<int64_t>(p.num_tiles, H.pair_clusters))
+                        : int(std::min<int64_t>(p.num_tiles, H.num_sms));
+  cudaError_t e =
+      launch_project(tmap_h, pair ? H.tmap_w_half : H.tmap_w, p, grid, pair, a.stream);
   if (e != cudaSuccess) return cuda_fail(e, "project launch");
   return HCR_OK;
 }
@@ -390,11 +399,17 @@ hcr_status hcr_create(const hcr_model_dims* dims, const void* const* gamma,
 
   st = encode_3d(&H.tmap_w, H.w_packed, d.dtype, uint64_t(d.d_model), uint64_t(2) * d_kv,
                  uint64_t(d.n_layers), kBlockN, "packed weights");
+  if (st == HCR_OK)
+    st = encode_3d(&H.tmap_w_half, H.w_packed, d.dtype, uint64_t(d.d_model), uint64_t(2) * d_kv,
+                   uint64_t(d.n_layers), kBlockN / 2, "packed weights (pair)");
   if (st != HCR_OK) {
     free_handle(H);
     delete h;
     return st;
   }
+  // How many CTA pairs fit at once; without any, restores use single CTAs.
+  H.pair_clusters = std::max(0, project_pair_clusters(d.dtype));
+  cudaGetLastError();
   *out = h;
   return HCR_OK;
 }
@@ -478,6 +493,15 @@ hcr_status hcr_check_device_error(hcr_handle* h, void* stream, uint32_t* flags) 
 }
 
 int32_t hcr_num_sms(const hcr_handle* h) { return h ? h->impl.num_sms : 0; }
+
+hcr_status hcr_debug_set_variant(hcr_handle* h, int32_t variant) {
+  if (!h) return fail(HCR_ERR_INVALID_ARG, "handle is NULL");
+  if (variant < 0 || variant > 2) return fail(HCR_ERR_INVALID_ARG, "variant must be 0, 1 or 2");
+  if (variant == 2 && h->impl.pair_clusters <= 0)
+    return fail(HCR_ERR_UNSUPPORTED, "CTA pairs cannot be co-scheduled on this device");
+  h->impl.variant = variant;
+  return HCR_OK;
+}
 
 hcr_status hcr_debug_set_stall(hcr_handle* h, int32_t enable) {
   if (!h) return fail(HCR_ERR_INVALID_ARG, "handle is NULL");

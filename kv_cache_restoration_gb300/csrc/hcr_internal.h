@@ -19,7 +19,9 @@ constexpr int kBlockM = 128;           // tokens per tile (TMEM lanes)
 constexpr int kBlockN = 256;           // K||V columns per tile (TMEM columns per accumulator)
 constexpr int kBlockK = 64;            // 64 x 2 bytes = one 128-byte swizzle row
 constexpr int kUmmaK = 16;             // K of one tcgen05.mma kind::f16
-constexpr int kStages = 4;             // TMA -> MMA shared-memory ring depth
+constexpr int kStages = 4;             // TMA -> MMA ring depth, single-CTA variant (48 KB stages)
+constexpr int kStagesPair = 6;         // ring depth per CTA, CTA-pair variant (32 KB stages)
+constexpr int kStagesMax = 6;
 constexpr int kAccums = 2;             // TMEM accumulators (epilogue overlaps next mainloop)
 constexpr int kTileBytesA = kBlockM * kBlockK * 2;
 constexpr int kTileBytesB = kBlockN * kBlockK * 2;
@@ -27,7 +29,12 @@ constexpr int kStageBytes = kTileBytesA + kTileBytesB;
 constexpr int kProjectThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kEpilogueWarps = 4;
 constexpr int kGroupM = 16;            // m-tiles per raster group (L2 reuse of hidden rows)
-constexpr size_t kProjectSmemBytes = size_t(kStages) * kStageBytes + 1024;  // + align slack
+// dynamic shared memory of either variant (both rings are 192 KB) + alignment slack
+constexpr size_t kProjectSmemBytes =
+    (size_t(kStages) * kStageBytes > size_t(kStagesPair) * (kTileBytesA + kTileBytesB / 2)
+         ? size_t(kStages) * kStageBytes
+         : size_t(kStagesPair) * (kTileBytesA + kTileBytesB / 2)) +
+    1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded pipeline waits: 2 s
 
 // tcgen05 instruction descriptor for kind::f16, fp32 accumulate, both
@@ -52,7 +59,10 @@ struct Handle {
   float2* rope_tab = nullptr;  // [max_position][head_dim/2] (cos, sin), or null
   uint32_t* err = nullptr;     // device error word (HCR_DEVERR_* bits)
   CUtensorMap tmap_w;          // 3-D map over w_packed: (d, 2*d_kv, L), box (64, 256, 1)
-  uint32_t debug_stall = 0;    // test hook: see hcr_debug_withhold_first_load
+  CUtensorMap tmap_w_half;     // same tensor, box (64, 128, 1): half a tile per CTA of a pair
+  int pair_clusters = 0;       // co-resident CTA pairs of the pair variant (0: unavailable)
+  uint32_t debug_stall = 0;    // test hook: see hcr_debug_set_stall
+  int32_t variant = 0;         // test hook: 0 auto, 1 single CTAs, 2 CTA pairs
 };
 
 // ---------------------------------------------------------------------------
@@ -126,7 +136,9 @@ hcr_status set_last_error(hcr_status s, const char* fmt, ...);
 // Launchers (return cudaGetLastError() of the launch).
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t s);
 cudaError_t launch_project(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
-                           const ProjectParams& p, int grid, cudaStream_t s);
+                           const ProjectParams& p, int grid, bool pair, cudaStream_t s);
+// Co-resident clusters of the CTA-pair variant on the current device (< 0 on error).
+int project_pair_clusters(int dtype);
 cudaError_t launch_pack_weights(const void* w_k, const void* w_v, const void* gamma, void* dst,
                                 int d_kv, int d, int dtype, cudaStream_t s);
 cudaError_t launch_column_constants(const void* w_packed, const void* w_k, const void* w_v,

@@ -18,12 +18,17 @@
 //
 // Warp roles (192 threads, one CTA per SM):
 //   warp 0      one lane issues TMA loads of hidden and weight tiles into a
-//               kStages-deep shared-memory ring;
+//               shared-memory ring;
 //   warp 1      allocates TMEM (2 accumulators x 256 fp32 columns) and one
-//               lane issues tcgen05.mma (M=128, N=256, K=16) for each stage;
+//               lane issues tcgen05.mma (K=16) for each stage;
 //   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (each warp
 //               owns one 32-lane TMEM quadrant = 32 tokens), overlapping the
 //               MMA of the next tile into the other accumulator.
+// Two variants: single CTAs with 128x256 tiles (cta_group::1, 4 stages of
+// 48 KB), and CTA pairs with 256x256 tiles (cta_group::2, 6 stages of 32 KB
+// per CTA).  The pair halves each SM's share of the weight tile, which cuts
+// shared-memory traffic per MMA by a third; the host picks the pair for
+// restores of more than 128 tokens.
 // Every pipeline wait is bounded (kWaitLimitNs); on expiry the kernel sets
 // HCR_DEVERR_TIMEOUT, stops all roles, drains in-flight copies and MMAs with
 // a bounded wait, frees TMEM and returns.
@@ -58,8 +63,8 @@ __device__ __forceinline__ TileCoord tile_coord(int64_t tile, const ProjectParam
 }
 
 struct __align__(8) PipeState {
-  uint64_t full[kStages];    // TMA -> MMA: stage filled
-  uint64_t empty[kStages];   // MMA -> TMA: stage consumed
+  uint64_t full[kStagesMax];    // TMA -> MMA: stage filled
+  uint64_t empty[kStagesMax];   // MMA -> TMA: stage consumed
   uint64_t tfull[kAccums];   // MMA -> epilogue: accumulator complete
   uint64_t tempty[kAccums];  // epilogue -> MMA: accumulator drained
   uint64_t drain;            // MMA completion on shutdown
@@ -118,41 +123,67 @@ __device__ __forceinline__ void store16(uint16_t* dst, const float (&x)[16]) {
   reinterpret_cast<uint4*>(dst)[1] = hi;
 }
 
-template <int DT>
+// Per-variant tiling.  Single: one CTA computes a 128x256 tile with
+// cta_group::1.  Pair: a cluster of two CTAs computes a 256x256 tile with one
+// cta_group::2 MMA stream; each CTA stages its own 128 rows of A and half of
+// B (128 rows), so a stage is 32 KB instead of 48 KB and six fit.
+template <bool PAIR>
+struct Tiling {
+  static constexpr int kStages = PAIR ? ::hcr::kStagesPair : ::hcr::kStages;
+  static constexpr int kRowsB = PAIR ? kBlockN / 2 : kBlockN;   // B rows staged per CTA
+  static constexpr int kTileM = PAIR ? 2 * kBlockM : kBlockM;   // token rows per tile
+  static constexpr int kBytesB = kRowsB * kBlockK * 2;
+  static constexpr int kStageBytes = kTileBytesA + kBytesB;
+};
+
+template <int DT, bool PAIR>
 __global__ void __launch_bounds__(kProjectThreads, 1)
     project_kernel(const __grid_constant__ CUtensorMap tmap_h,
                    const __grid_constant__ CUtensorMap tmap_w, const ProjectParams p) {
+  using Tl = Tiling<PAIR>;
+  constexpr int S = Tl::kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ PipeState ps;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* smem_a = smem;                                   // kStages x [128][64]
-  uint8_t* smem_b = smem + size_t(kStages) * kTileBytesA;   // kStages x [256][64]
+  uint8_t* smem_a = smem;                                   // S x [128][64]
+  uint8_t* smem_b = smem + size_t(S) * kTileBytesA;         // S x [kRowsB][64]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int32_t* abort = &ps.abort;
+  // In a pair, CTA rank 0 (the leader) issues every MMA for both CTAs.
+  const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int64_t unit = PAIR ? int64_t(blockIdx.x >> 1) : int64_t(blockIdx.x);
+  const int64_t units = PAIR ? int64_t(gridDim.x >> 1) : int64_t(gridDim.x);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       ptx::mbar_init(ptx::smem_u32(&ps.full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&ps.empty[s]), 1);
     }
     for (int a = 0; a < kAccums; ++a) {
       ptx::mbar_init(ptx::smem_u32(&ps.tfull[a]), 1);
-      ptx::mbar_init(ptx::smem_u32(&ps.tempty[a]), kEpilogueWarps);
+      ptx::mbar_init(ptx::smem_u32(&ps.tempty[a]), PAIR ? 2 * kEpilogueWarps : kEpilogueWarps);
     }
     ptx::mbar_init(ptx::smem_u32(&ps.drain), 1);
     ps.abort = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(&ps.tmem_base), kAccums * kBlockN);
-    ptx::tmem_relinquish();
+    if constexpr (PAIR) {
+      ptx::tmem_alloc_pair(ptx::smem_u32(&ps.tmem_base), kAccums * kBlockN);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(&ps.tmem_base), kAccums * kBlockN);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) ptx::cluster_sync();   // peer barriers initialised before any remote use
   ptx::tc_fence_after();
   const uint32_t tmem_base = ps.tmem_base;
 
@@ -165,23 +196,37 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int64_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int64_t tile = unit; ok && tile < p.num_tiles; tile += units) {
         const TileCoord c = tile_coord(tile, p);
+        const int row_a = c.m * Tl::kTileM + int(rank) * kBlockM;
+        const int row_b = c.n * kBlockN + int(rank) * Tl::kRowsB;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase(ptx::smem_u32(&ps.empty[stage]), phase ^ 1u, abort, p.err)) {
             ok = false;
             break;
           }
           const uint32_t full = ptx::smem_u32(&ps.full[stage]);
-          ptx::mbar_arrive_expect_tx(full, kStageBytes);
-          if (!(p.debug_stall && issued == 0)) {
-            ptx::tma_load_3d(ptx::smem_u32(smem_a + size_t(stage) * kTileBytesA), &tmap_h, full,
-                             kb * kBlockK, c.m * kBlockM, c.l);
-            ptx::tma_load_3d(ptx::smem_u32(smem_b + size_t(stage) * kTileBytesB), &tmap_w, full,
-                             kb * kBlockK, c.n * kBlockN, p.layer_begin + c.l);
+          const uint32_t dst_a = ptx::smem_u32(smem_a + size_t(stage) * kTileBytesA);
+          const uint32_t dst_b = ptx::smem_u32(smem_b + size_t(stage) * Tl::kBytesB);
+          if constexpr (PAIR) {
+            // both CTAs' bytes complete on the leader's barrier; only the
+            // leader arrives (with the pair's total byte count)
+            if (leader) ptx::mbar_arrive_expect_tx(full, 2 * Tl::kStageBytes);
+            const uint32_t full_leader = ptx::mapa_shared(full, 0);
+            if (!(p.debug_stall && issued == 0)) {
+              ptx::tma_load_3d_pair(dst_a, &tmap_h, full_leader, kb * kBlockK, row_a, c.l);
+              ptx::tma_load_3d_pair(dst_b, &tmap_w, full_leader, kb * kBlockK, row_b,
+                                    p.layer_begin + c.l);
+            }
+          } else {
+            ptx::mbar_arrive_expect_tx(full, Tl::kStageBytes);
+            if (!(p.debug_stall && issued == 0)) {
+              ptx::tma_load_3d(dst_a, &tmap_h, full, kb * kBlockK, row_a, c.l);
+              ptx::tma_load_3d(dst_b, &tmap_w, full, kb * kBlockK, row_b, p.layer_begin + c.l);
+            }
           }
           ++issued;
-          if (++stage == kStages) {
+          if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
@@ -190,14 +235,14 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_f16(DT, kBlockM, kBlockN);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = make_idesc_f16(DT, Tl::kTileM, kBlockN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int64_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int64_t tile = unit; ok && tile < p.num_tiles; tile += units) {
         if (!wait_phase(ptx::smem_u32(&ps.tempty[acc]), acc_phase ^ 1u, abort, p.err)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * kBlockN);
@@ -208,38 +253,50 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
           }
           ptx::tc_fence_after();
           const uint32_t a0 = ptx::smem_u32(smem_a + size_t(stage) * kTileBytesA);
-          const uint32_t b0 = ptx::smem_u32(smem_b + size_t(stage) * kTileBytesB);
+          const uint32_t b0 = ptx::smem_u32(smem_b + size_t(stage) * Tl::kBytesB);
 #pragma unroll
           for (int k = 0; k < kBlockK / kUmmaK; ++k) {
-            ptx::mma_f16(d_tmem, ptx::sw128_kmajor_desc(a0 + k * kUmmaK * 2),
-                         ptx::sw128_kmajor_desc(b0 + k * kUmmaK * 2), idesc,
-                         (kb | k) != 0 ? 1u : 0u);
+            const uint64_t da = ptx::sw128_kmajor_desc(a0 + k * kUmmaK * 2);
+            const uint64_t db = ptx::sw128_kmajor_desc(b0 + k * kUmmaK * 2);
+            if constexpr (PAIR)
+              ptx::mma_f16_pair(d_tmem, da, db, idesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              ptx::mma_f16(d_tmem, da, db, idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          ptx::mma_commit(ptx::smem_u32(&ps.empty[stage]));
-          if (++stage == kStages) {
+          if constexpr (PAIR)
+            ptx::mma_commit_pair_multicast(ptx::smem_u32(&ps.empty[stage]), 0x3);
+          else
+            ptx::mma_commit(ptx::smem_u32(&ps.empty[stage]));
+          if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        ptx::mma_commit(ptx::smem_u32(&ps.tfull[acc]));
+        if constexpr (PAIR)
+          ptx::mma_commit_pair_multicast(ptx::smem_u32(&ps.tfull[acc]), 0x3);
+        else
+          ptx::mma_commit(ptx::smem_u32(&ps.tfull[acc]));
         if (++acc == kAccums) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       // Every MMA this thread issued has completed once `drain` flips.
-      ptx::mma_commit(ptx::smem_u32(&ps.drain));
+      if constexpr (PAIR)
+        ptx::mma_commit_pair_multicast(ptx::smem_u32(&ps.drain), 0x1);
+      else
+        ptx::mma_commit(ptx::smem_u32(&ps.drain));
       drain_wait(ptx::smem_u32(&ps.drain), 0);
     }
   } else {
     // ------------------------------------------------------------- epilogue
     const int quad = warp & 3;               // TMEM lanes [32*quad, 32*quad+32)
-    const int row = quad * 32 + lane;        // token row within the tile
+    const int row = quad * 32 + lane;        // token row within this CTA's 128 rows
     const int half = p.head_dim >> 1;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    for (int64_t tile = unit; tile < p.num_tiles; tile += units) {
       const TileCoord c = tile_coord(tile, p);
       int ok = 0;
       if (lane == 0) ok = wait_phase(ptx::smem_u32(&ps.tfull[acc]), acc_phase, abort, p.err);
@@ -247,7 +304,7 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
       if (!ok) break;
       ptx::tc_fence_after();
 
-      const int t = c.m * kBlockM + row;
+      const int t = c.m * Tl::kTileM + int(rank) * kBlockM + row;
       bool valid = t < p.n_tokens;
       int64_t slot = -1;
       int pos = 0;
@@ -323,7 +380,12 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ps.tempty[acc]));
+      if (lane == 0) {
+        if constexpr (PAIR)   // the leader's MMA reuses the accumulator in both CTAs
+          ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&ps.tempty[acc]), 0));
+        else
+          ptx::mbar_arrive(ptx::smem_u32(&ps.tempty[acc]));
+      }
       if (++acc == kAccums) {
         acc = 0;
         acc_phase ^= 1u;
@@ -333,43 +395,103 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (*abort) {
-    // Some role gave up: loads the producer armed may still be landing in
-    // shared memory.  They are among its last kStages; wait for each (bounded)
-    // before the CTA releases its memory.
-    if (warp == 0 && lane == 0) {
-      const int64_t first = issued > kStages ? issued - kStages : 0;
+  if constexpr (PAIR) {
+    // Both CTAs have left their roles.  The leader's full barriers count both
+    // CTAs' loads, so the leader waits (bounded; immediate unless a role gave
+    // up) for its last S stages before either CTA releases its memory.
+    ptx::cluster_sync();
+    if (leader && warp == 0 && lane == 0) {
+      const int64_t first = issued > S ? issued - S : 0;
       for (int64_t i = first; i < issued; ++i)
-        drain_wait(ptx::smem_u32(&ps.full[i % kStages]), uint32_t((i / kStages) & 1));
+        drain_wait(ptx::smem_u32(&ps.full[i % S]), uint32_t((i / S) & 1));
     }
-    __syncthreads();
+    ptx::cluster_sync();
+    if (warp == 1) {
+      ptx::tc_fence_after();
+      ptx::tmem_dealloc_pair(tmem_base, kAccums * kBlockN);
+    }
+  } else {
+    if (*abort) {
+      // Some role gave up: loads the producer armed may still be landing in
+      // shared memory.  They are among its last S; wait for each (bounded)
+      // before the CTA releases its memory.
+      if (warp == 0 && lane == 0) {
+        const int64_t first = issued > S ? issued - S : 0;
+        for (int64_t i = first; i < issued; ++i)
+          drain_wait(ptx::smem_u32(&ps.full[i % S]), uint32_t((i / S) & 1));
+      }
+      __syncthreads();
+    }
+    if (warp == 1) {
+      ptx::tc_fence_after();
+      ptx::tmem_dealloc(tmem_base, kAccums * kBlockN);
+    }
   }
-  if (warp == 1) {
-    ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, kAccums * kBlockN);
+}
+
+template <int DT, bool PAIR>
+cudaError_t launch_variant(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
+                           const ProjectParams& p, int grid, cudaStream_t s) {
+  auto kernel = project_kernel<DT, PAIR>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(kProjectSmemBytes));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kProjectThreads);
+  cfg.dynamicSmemBytes = kProjectSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
   }
+  return cudaLaunchKernelEx(&cfg, kernel, tmap_h, tmap_w, p);
+}
+
+template <int DT>
+int max_pair_clusters() {
+  auto kernel = project_kernel<DT, true>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(kProjectSmemBytes)) != cudaSuccess)
+    return -1;
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(sms & ~1));
+  cfg.blockDim = dim3(kProjectThreads);
+  cfg.dynamicSmemBytes = kProjectSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return -1;
+  return n;
 }
 
 }  // namespace
 
 cudaError_t launch_project(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
-                           const ProjectParams& p, int grid, cudaStream_t s) {
-  if (p.dtype == HCR_DTYPE_BF16) {
-    cudaError_t e = cudaFuncSetAttribute(project_kernel<HCR_DTYPE_BF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kProjectSmemBytes));
-    if (e != cudaSuccess) return e;
-    project_kernel<HCR_DTYPE_BF16><<<grid, kProjectThreads, kProjectSmemBytes, s>>>(tmap_h, tmap_w,
-                                                                                  p);
-  } else {
-    cudaError_t e = cudaFuncSetAttribute(project_kernel<HCR_DTYPE_FP16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kProjectSmemBytes));
-    if (e != cudaSuccess) return e;
-    project_kernel<HCR_DTYPE_FP16><<<grid, kProjectThreads, kProjectSmemBytes, s>>>(tmap_h, tmap_w,
-                                                                                  p);
-  }
-  return cudaGetLastError();
+                           const ProjectParams& p, int grid, bool pair, cudaStream_t s) {
+  if (p.dtype == HCR_DTYPE_BF16)
+    return pair ? launch_variant<HCR_DTYPE_BF16, true>(tmap_h, tmap_w, p, grid, s)
+                : launch_variant<HCR_DTYPE_BF16, false>(tmap_h, tmap_w, p, grid, s);
+  return pair ? launch_variant<HCR_DTYPE_FP16, true>(tmap_h, tmap_w, p, grid, s)
+              : launch_variant<HCR_DTYPE_FP16, false>(tmap_h, tmap_w, p, grid, s);
+}
+
+int project_pair_clusters(int dtype) {
+  return dtype == HCR_DTYPE_BF16 ? max_pair_clusters<HCR_DTYPE_BF16>()
+                                 : max_pair_clusters<HCR_DTYPE_FP16>();
 }
 
 }  // namespace hcr

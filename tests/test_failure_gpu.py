@@ -12,10 +12,12 @@ from workloads import configs as C
 pytestmark = pytest.mark.gpu
 
 
-def test_stalled_pipeline_times_out_and_context_survives(cuda_device):
+@pytest.mark.parametrize("variant", [1, 2], ids=["single", "pair"])
+def test_stalled_pipeline_times_out_and_context_survives(cuda_device, variant):
     from kv_cache_restoration_gb300 import binding as B
     w = C.get("tiny")
     case = Hn.make_case(w, cuda_device)
+    assert B.hcr_debug_set_variant(case.restorer.handle, variant) == B.HCR_OK
     assert B.hcr_debug_set_stall(case.restorer.handle, True) == B.HCR_OK
     t0 = time.monotonic()
     Hn.run(case)

@@ -38,11 +38,34 @@ SMALL_CASES = [
 ]
 
 
+VARIANTS = {"auto": 0, "single": 1, "pair": 2}
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
 @pytest.mark.parametrize("w", SMALL_CASES, ids=[w.name for w in SMALL_CASES])
-def test_small_full(cuda_device, w):
-    case = Hn.run(Hn.make_case(w, cuda_device))
+def test_small_full(cuda_device, w, variant):
+    from kv_cache_restoration_gb300 import binding as B
+    case = Hn.make_case(w, cuda_device)
+    assert B.hcr_debug_set_variant(case.restorer.handle, VARIANTS[variant]) == 0
+    Hn.run(case)
     assert case.status == 0, (case.status, case.flags)
     Hn.compare(case)
+
+
+def test_variants_agree(cuda_device):
+    """Single-CTA and CTA-pair tiles restore the same values (compared bit for
+    bit; a difference would show as a count of differing elements)."""
+    from kv_cache_restoration_gb300 import binding as B
+    w = SMALL_CASES[1]
+    a = Hn.make_case(w, cuda_device)
+    B.hcr_debug_set_variant(a.restorer.handle, 1)
+    Hn.run(a)
+    b = Hn.make_case(w, cuda_device, params=a.params, restorer=a.restorer)
+    B.hcr_debug_set_variant(b.restorer.handle, 2)
+    Hn.run(b)
+    for c in ("k_cache", "v_cache"):
+        diff = int((getattr(a, c).view(torch.int16) != getattr(b, c).view(torch.int16)).sum())
+        assert diff == 0, f"{c}: {diff} elements differ between variants"
 
 
 def test_empty_restore_is_a_noop(cuda_device):

@@ -193,6 +193,37 @@ hcr_status hcr_restore_project(hcr_handle* h, const void* hidden, int32_t layer_
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * hcr_restore_streamed -- the layer-pipelined restore from host memory.
+ *
+ * The HCache episode (cue 15) overlaps the transfer of layer N+1's hidden
+ * states with the projection of layer N.  This call does that for hidden
+ * states held in host memory: it copies them to the device one chunk of
+ * layers_per_chunk layers at a time, on a copy stream owned by the handle,
+ * into a ring of chunk-sized slots carved from `staging`, and restores each
+ * chunk on `stream` (exactly as hcr_restore would) as soon as its copy has
+ * landed; a slot is refilled only after the restore that read it finished.
+ *
+ * hidden_host: HOST [layer_end-layer_begin][n_tokens][d_model]; pinned
+ *              (page-locked) memory lets the copies overlap the restores.
+ * staging:     DEVICE, 256-byte aligned, owned by the caller; its size
+ *              decides the ring: min(8, staging_bytes / chunk bytes) slots,
+ *              at least one (one slot restores correctly but serialises).
+ * workspace:   as hcr_restore, sized for one chunk:
+ *              hcr_workspace_bytes(h, n_tokens, layers_per_chunk).
+ * Every other argument is as in hcr_restore (k_cache and v_cache are the
+ * base of layer layer_begin).  Returns after enqueueing; the restore is
+ * complete when `stream` reaches this point.  Calls through one handle are
+ * serialised on the host while they enqueue.
+ */
+hcr_status hcr_restore_streamed(hcr_handle* h, const void* hidden_host, int32_t layer_begin,
+                                int32_t layer_end, int32_t n_req, int32_t n_tokens,
+                                const int32_t* cu_seqlens, const int32_t* start_pos,
+                                const int32_t* block_table, int32_t max_blocks_per_req,
+                                void* k_cache, void* v_cache, const hcr_cache_layout* layout,
+                                void* staging, size_t staging_bytes, int32_t layers_per_chunk,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * hcr_restore_no_alloc -- hcr_restore without a caller-provided workspace.
  *
  * The paper has no counterpart to this call; it exists for callers of this

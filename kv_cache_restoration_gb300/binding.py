@@ -78,6 +78,9 @@ lib.hcr_workspace_bytes.restype = ctypes.c_size_t
 for _name in ("hcr_restore", "hcr_restore_prepare", "hcr_restore_project"):
     getattr(lib, _name).argtypes = _RESTORE_ARGTYPES
     getattr(lib, _name).restype = ctypes.c_int
+lib.hcr_restore_streamed.argtypes = _RESTORE_ARGTYPES[:13] + [_vp, ctypes.c_size_t, _i32, _vp,
+                                                            ctypes.c_size_t, _vp]
+lib.hcr_restore_streamed.restype = ctypes.c_int
 lib.hcr_restore_no_alloc.argtypes = _RESTORE_ARGTYPES[:13] + [_vp]
 lib.hcr_restore_no_alloc.restype = ctypes.c_int
 HCR_NO_ALLOC_SCRATCH_BYTES = 16 << 20
@@ -190,6 +193,22 @@ def hcr_restore_project(handle, hidden, layer_begin, layer_end, n_req, n_tokens,
                          layer_begin, layer_end, n_req, n_tokens, cu_seqlens, start_pos,
                          block_table, max_blocks_per_req, k_cache, v_cache, layout, workspace,
                          workspace_bytes, stream, check)
+
+
+def hcr_restore_streamed(handle, hidden_host, layer_begin, layer_end, n_req, n_tokens,
+                         cu_seqlens, start_pos, block_table, max_blocks_per_req, k_cache, v_cache,
+                         layout, staging, staging_bytes, layers_per_chunk, workspace,
+                         workspace_bytes, stream=None, *, check: bool = True) -> int:
+    """Layer-pipelined restore: hidden states in (pinned) host memory, copied in
+    chunks of layers into a device staging ring while earlier chunks restore."""
+    st = lib.hcr_restore_streamed(
+        handle, _ptr(hidden_host), layer_begin, layer_end, n_req, n_tokens, _ptr(cu_seqlens),
+        _ptr(start_pos), _ptr(block_table), max_blocks_per_req, _ptr(k_cache), _ptr(v_cache),
+        ctypes.byref(layout) if layout is not None else None, _ptr(staging), staging_bytes,
+        layers_per_chunk, _ptr(workspace), workspace_bytes, _stream_ptr(stream))
+    if check:
+        _check(st, "hcr_restore_streamed")
+    return st
 
 
 def hcr_restore_no_alloc(handle, hidden, layer_begin, layer_end, n_req, n_tokens, cu_seqlens,

@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhcr.so")
 
-SOURCES = ["hcr_api.cu", "hcr_prepare.cu", "hcr_project.cu", "hcr_no_alloc.cu"]
+SOURCES = ["hcr_api.cu", "hcr_prepare.cu", "hcr_project.cu", "hcr_no_alloc.cu",
+           "hcr_streamed.cu"]
 HEADERS = ["hcr_internal.h", "ptx.cuh"]
 
 NVCC_FLAGS = [

@@ -253,6 +253,7 @@ hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
 }
 
 void free_handle(Handle& H) {
+  release_streamed(H);
   cudaFree(H.w_packed);
   cudaFree(H.col_sum);
   cudaFree(H.col_bias);

@@ -46,6 +46,10 @@ constexpr uint32_t make_idesc_f16(int dtype, int m, int n) {
          (uint32_t(m >> 4) << 24);
 }
 
+constexpr int kMaxStagingSlots = 8;    // staging ring of the layer-pipelined restore
+
+struct StreamedRes;  // copy stream + events of hcr_restore_streamed (hcr_streamed.cu)
+
 // ---------------------------------------------------------------------------
 // Handle
 // ---------------------------------------------------------------------------
@@ -63,7 +67,10 @@ struct Handle {
   int pair_clusters = 0;       // co-resident CTA pairs of the pair variant (0: unavailable)
   uint32_t debug_stall = 0;    // test hook: see hcr_debug_set_stall
   int32_t variant = 0;         // test hook: 0 auto, 1 single CTAs, 2 CTA pairs
+  StreamedRes* streamed = nullptr;  // created on the first hcr_restore_streamed call
 };
+
+void release_streamed(Handle& H);
 
 // ---------------------------------------------------------------------------
 // Workspace layout (all offsets 256-byte aligned)

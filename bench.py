@@ -130,6 +130,23 @@ def profiled_traffic(workload_base: str, n_layers: int):
     return (rec["dram_bytes_read"] + rec["dram_bytes_write"]) * n_layers / rec["captured_layers"]
 
 
+def reduce_max_over_ranks(values, device=None):
+    """Element-wise max of a list of floats over all ranks (the slowest rank's
+    times); identity when torch.distributed is not initialised."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_tokens_per_s(world: int, tokens_per_rank: int, t_step_max: float) -> float:
+    """Units all ranks processed divided by the slowest rank's step time."""
+    return world * tokens_per_rank / t_step_max
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_child(args):
     """Runs in a fresh interpreter: time the oracle on a bounded sample of the
@@ -298,10 +315,8 @@ def gpu_arm(args, rank, world, local_rank):
         h2d_gbs = hidden_host.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9
 
     t_step = total_ms / 1e3 / args.steps
-    if world > 1:
-        t = torch.tensor([t_step, proj_ms, prep_ms, e2e_s], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step, proj_ms, prep_ms, e2e_s = t.tolist()
+    t_step, proj_ms, prep_ms, e2e_s = reduce_max_over_ranks([t_step, proj_ms, prep_ms, e2e_s],
+                                                            device)
     return dict(w=w, t_step=t_step, proj_ms=proj_ms, prep_ms=prep_ms, e2e_s=e2e_s, h2d=h2d,
                 clocks=clk.summary(), launches=2 * args.steps, h2d_gbs=h2d_gbs, chunk=chunk)
 
@@ -386,7 +401,7 @@ def main():
         return
 
     t = res["t_step"]
-    tokens_s = world * w.n_tokens / t
+    tokens_s = whole_job_tokens_per_s(world, w.n_tokens, t)
     kv_gbs = world * kv_b / t / 1e9
     proj_s = res["proj_ms"] / 1e3
     t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
@@ -430,7 +445,8 @@ def main():
         "stage_ms": {"prepare": res["prep_ms"], "project": res["proj_ms"]},
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": ({"value": world * w.n_tokens / res["e2e_s"], "unit": "tokens/s",
+        "e2e": ({"value": whole_job_tokens_per_s(world, w.n_tokens, res["e2e_s"]),
+                 "unit": "tokens/s",
                  "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": 4,
                  "ms_per_step": res["e2e_s"] * 1e3,
                  "api": f"hcr_restore_streamed, {res['chunk']}-layer chunks, "

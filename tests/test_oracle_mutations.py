@@ -161,3 +161,56 @@ def test_unmutated_oracle_passes_every_pin():
     for pin, args in _all_pins():
         pin(*args)
     pins.pin_kv_bytes(R, _facts())
+
+
+# ----------------------------------------------------------------------------- save side
+from oracle import save as S  # noqa: E402
+from tests import test_oracle_save as TS  # noqa: E402
+
+SAVE_ORIG = S.chunk_placement
+
+
+def _offset_from_index(cu_seqlens, start_pos, chunk_table, chunk_tokens, num_chunks=None):
+    pl = SAVE_ORIG(cu_seqlens, start_pos, chunk_table, chunk_tokens, num_chunks)
+    idx = pl.pos - np.asarray(start_pos)[pl.request]
+    pl.offset = idx % chunk_tokens
+    return pl
+
+
+def _chunk_from_index(cu_seqlens, start_pos, chunk_table, chunk_tokens, num_chunks=None):
+    pl = SAVE_ORIG(cu_seqlens, start_pos, chunk_table, chunk_tokens, num_chunks)
+    idx = pl.pos - np.asarray(start_pos)[pl.request]
+    pl.chunk = np.asarray(chunk_table)[pl.request, idx // chunk_tokens]
+    return pl
+
+
+def _save_layer_inner(hidden, layer_begin, n_layers, cu_seqlens, start_pos, chunk_table,
+                      chunk_tokens, num_chunks, buf=None):
+    # mistake: token-major inside the chunk ([C][L][d]) written into the [L][C][d] store
+    d = np.asarray(hidden[0]).shape[-1]
+    if buf is None:
+        buf = np.full((num_chunks, n_layers, chunk_tokens, d), np.nan)
+    pl = SAVE_ORIG(cu_seqlens, start_pos, chunk_table, chunk_tokens, num_chunks)
+    flat = buf.reshape(num_chunks, -1, d)
+    for i, h in enumerate(hidden):
+        flat[pl.chunk, pl.offset * n_layers + layer_begin + i] = h
+    return buf
+
+
+SAVE_PINS = [TS.test_hand_worked_layout, lambda: TS.test_against_chunk_walk(4),
+             TS.test_round_trip_and_layer_ranges, TS.test_decode_steps_equal_one_save]
+
+
+@pytest.mark.parametrize("attr,mutant", [("chunk_placement", _offset_from_index),
+                                         ("chunk_placement", _chunk_from_index),
+                                         ("save_chunks", _save_layer_inner)],
+                         ids=["offset_from_index", "chunk_from_index", "token_major_chunk"])
+def test_planted_save_mistake_is_caught(monkeypatch, attr, mutant):
+    monkeypatch.setattr(S, attr, mutant)
+    failed = 0
+    for pin in SAVE_PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            failed += 1
+    assert failed, f"no pin caught {mutant.__name__}"

@@ -321,12 +321,105 @@ def gpu_arm(args, rank, world, local_rank):
                 clocks=clk.summary(), launches=2 * args.steps, h2d_gbs=h2d_gbs, chunk=chunk)
 
 
+def save_arm(args):
+    """Save side: layer inputs into 64-token, token-before-layer chunks
+    (hcr_save_hidden), into device memory and into pinned host memory, for a
+    whole 4096-token prompt and for one decode step of 64 requests."""
+    from dataclasses import replace as dc_replace
+
+    import torch
+
+    import __graft_entry__
+    __graft_entry__._build_module().build()
+    from kv_cache_restoration_gb300 import Restorer, make_dims
+    from kv_cache_restoration_gb300 import binding as B
+    from workloads import configs as C
+    from workloads import generate as G
+
+    device = torch.device("cuda", 0)
+    w = C.get(args.workload)
+    if args.layers:
+        w = C.with_layers(w, args.layers)
+    s = w.shape
+    L, T, d = s.n_layers, w.n_tokens, s.d_model
+    case = G.device_inputs(w, device, gen_device=device)
+    r = Restorer(make_dims(L, d, s.n_heads, s.n_kv_heads, s.head_dim, s.norm, s.norm_eps,
+                           s.rope, s.rope_theta, w.rope_positions, s.dtype, s.kv_bias),
+                 case.params)
+    case.params = None
+    stream = torch.cuda.current_stream(device)
+    peaks, peak_kind = load_peaks()
+
+    def timed(fn, steps, warmup):
+        for _ in range(warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        if r.check(stream)[0] != 0:
+            raise RuntimeError("save reported a device error")
+        return e0.elapsed_time(e1) / 1e3 / steps
+
+    lay = G.request_layout(dc_replace(w, block_size=64))
+    table = torch.as_tensor(lay.block_table, device=device)
+    n = lay.num_blocks
+    shape = (n, L, 64, d)
+    dev_store = torch.empty(shape, dtype=G.TORCH_DTYPE[s.dtype], device=device)
+    host_store = torch.empty(shape, dtype=G.TORCH_DTYPE[s.dtype]).pin_memory()
+
+    def save_to(store, hidden, cu, start, tab, n_req, n_tok):
+        return lambda: B.hcr_save_hidden(r.handle, hidden, 0, L, n_req, n_tok, cu, start, tab,
+                                         int(tab.shape[1]), 64, store, int(store.shape[0]),
+                                         stream)
+
+    t_dev = timed(save_to(dev_store, case.hidden, case.cu, case.start, table, 1, T),
+                  args.steps, args.warmup)
+    t_host = timed(save_to(host_store, case.hidden, case.cu, case.start, table, 1, T),
+                   max(3, args.steps // 10), 2)
+    # one decode step: 64 requests at positions 4095, one token each, all layers
+    B_ = 64
+    dw = C.Workload("decode", s, (1,) * B_, (T - 1,) * B_)
+    dlay = G.request_layout(dc_replace(dw, block_size=64))
+    dtab = torch.as_tensor(dlay.block_table, device=device)
+    dstore = torch.empty((dlay.num_blocks, L, 64, d), dtype=G.TORCH_DTYPE[s.dtype],
+                         device=device)
+    dhid = case.hidden[:, :B_].contiguous()
+    dcu = torch.arange(B_ + 1, dtype=torch.int32, device=device)
+    dst_ = torch.full((B_,), T - 1, dtype=torch.int32, device=device)
+    t_dec = timed(save_to(dstore, dhid, dcu, dst_, dtab, B_, B_), args.steps, args.warmup)
+
+    moved = 2.0 * L * T * d * 2          # read + write, bytes
+    line = {
+        "op": "save", "metric": "saved tokens/s (all layers' inputs into 64-token chunks)",
+        "value": T / t_dev, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_dev * 1e3, "higher_is_better": True,
+        "dtype": s.dtype, "data": "synthetic",
+        "config": {"workload": f"{w.name}: {L} layers x {T} tokens x d={d}, chunks of 64"},
+        "roofline": {"bound": "hbm", "achieved": moved / t_dev / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": moved / t_dev / 1e9 / peaks["hbm_gbs"],
+                     "peak_source": f"{peak_kind} HBM copy bandwidth", "kernel": "save_kernel"},
+        "host_store": {"ms_per_step": t_host * 1e3, "tokens_per_s": T / t_host,
+                       "write_gbs": moved / 2 / t_host / 1e9},
+        "decode_step": {"requests": B_, "us_per_step": t_dec * 1e6,
+                        "achieved_gbs": 2.0 * L * B_ * d * 2 / t_dec / 1e9},
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--op", default="restore", choices=["restore", "save"],
+                    help="restore (the benchmark step) or save (hcr_save_hidden)")
     ap.add_argument("--workload", default="llama2-7b")
     ap.add_argument("--e2e-steps", type=int, default=30, help="0 skips the end-to-end leg")
     ap.add_argument("--e2e-chunk", type=int, default=4, help="layers per streamed chunk")
@@ -348,6 +441,8 @@ def main():
         return oracle_child(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.op == "save":
+        return save_arm(args)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -224,6 +224,41 @@ hcr_status hcr_restore_streamed(hcr_handle* h, const void* hidden_host, int32_t 
                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * hcr_save_hidden -- the save side: store layer inputs in fixed-size chunks.
+ *
+ * HCache episode, cue 16: generation produces hidden states layer before
+ * token (each decode step yields every layer's input for its new token),
+ * while a restore reads all tokens of one layer together; cue 22: they are
+ * kept in fixed 64-token chunks.  A chunk holds positions [C*k, C*k + C) of
+ * one request (logical chunk k = position / C) for ALL layers, laid out
+ *     chunk_store[id][layer][position % C][d_model]
+ * so inside a chunk each layer's tokens are contiguous (token before layer).
+ *
+ * hidden:       DEVICE [layer_end-layer_begin][n_tokens][d_model], 16-byte
+ *               aligned: row t of layer layer_begin+i.  A decode step is one
+ *               token per request; a prefill saves a whole prompt.
+ * n_req, n_tokens, cu_seqlens, start_pos: as in hcr_restore.
+ * chunk_table:  DEVICE int32 [n_req][max_chunks_per_req]; entry [r][k] is the
+ *               physical chunk of request r's positions [C*k, C*k + C).
+ * chunk_tokens: C, tokens per chunk (64 on the page).
+ * chunk_store:  [num_chunks][n_layers][C][d_model] in the handle's dtype,
+ *               16-byte aligned; device memory, or pinned (mapped) host
+ *               memory -- the stores then cross the host link directly,
+ *               with no separate snapshot copy.  Host memory the device
+ *               cannot address is rejected with HCR_ERR_INVALID_ARG.
+ * Only the slots of the given rows are written.  Rows whose chunk id or
+ * logical chunk is out of range are skipped and flagged
+ * (HCR_DEVERR_BLOCK_ID / HCR_DEVERR_LOGICAL_BLOCK; read them with
+ * hcr_check_device_error).  Enqueues one kernel on `stream`.
+ */
+hcr_status hcr_save_hidden(hcr_handle* h, const void* hidden, int32_t layer_begin,
+                           int32_t layer_end, int32_t n_req, int32_t n_tokens,
+                           const int32_t* cu_seqlens, const int32_t* start_pos,
+                           const int32_t* chunk_table, int32_t max_chunks_per_req,
+                           int32_t chunk_tokens, void* chunk_store, int32_t num_chunks,
+                           void* stream);
+
+/*
  * hcr_restore_no_alloc -- hcr_restore without a caller-provided workspace.
  *
  * The paper has no counterpart to this call; it exists for callers of this

@@ -81,6 +81,9 @@ for _name in ("hcr_restore", "hcr_restore_prepare", "hcr_restore_project"):
 lib.hcr_restore_streamed.argtypes = _RESTORE_ARGTYPES[:13] + [_vp, ctypes.c_size_t, _i32, _vp,
                                                             ctypes.c_size_t, _vp]
 lib.hcr_restore_streamed.restype = ctypes.c_int
+lib.hcr_save_hidden.argtypes = [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _vp,
+                                _i32, _vp]
+lib.hcr_save_hidden.restype = ctypes.c_int
 lib.hcr_restore_no_alloc.argtypes = _RESTORE_ARGTYPES[:13] + [_vp]
 lib.hcr_restore_no_alloc.restype = ctypes.c_int
 HCR_NO_ALLOC_SCRATCH_BYTES = 16 << 20
@@ -208,6 +211,19 @@ def hcr_restore_streamed(handle, hidden_host, layer_begin, layer_end, n_req, n_t
         layers_per_chunk, _ptr(workspace), workspace_bytes, _stream_ptr(stream))
     if check:
         _check(st, "hcr_restore_streamed")
+    return st
+
+
+def hcr_save_hidden(handle, hidden, layer_begin, layer_end, n_req, n_tokens, cu_seqlens,
+                    start_pos, chunk_table, max_chunks_per_req, chunk_tokens, chunk_store,
+                    num_chunks, stream=None, *, check: bool = True) -> int:
+    """Scatter layer inputs into fixed-size, token-before-layer chunks."""
+    st = lib.hcr_save_hidden(handle, _ptr(hidden), layer_begin, layer_end, n_req, n_tokens,
+                             _ptr(cu_seqlens), _ptr(start_pos), _ptr(chunk_table),
+                             max_chunks_per_req, chunk_tokens, _ptr(chunk_store), num_chunks,
+                             _stream_ptr(stream))
+    if check:
+        _check(st, "hcr_save_hidden")
     return st
 
 

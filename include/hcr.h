@@ -327,6 +327,16 @@ hcr_status hcr_debug_set_stall(hcr_handle* h, int32_t enable);
  */
 hcr_status hcr_debug_set_variant(hcr_handle* h, int32_t variant);
 
+/*
+ * hcr_debug_timeout_record -- diagnostics for HCR_ERR_TIMEOUT: synchronise
+ * `stream`, copy the record of the first pipeline wait that gave up since the
+ * last call into out[6] = {which wait (0: none), CTA, thread, a, b, parity}
+ * and clear it.  Which wait: 1 producer (stage free), 3 MMA (accumulator
+ * free), 4 MMA (stage full), 7 epilogue (accumulator full); a and b are the
+ * tile index and the k-block or accumulator.
+ */
+hcr_status hcr_debug_timeout_record(hcr_handle* h, void* stream, uint32_t out[6]);
+
 /* Static description of a status code. */
 const char* hcr_status_string(hcr_status s);
 

@@ -95,6 +95,8 @@ lib.hcr_last_error.argtypes = []
 lib.hcr_last_error.restype = ctypes.c_char_p
 lib.hcr_num_sms.argtypes = [_vp]
 lib.hcr_num_sms.restype = _i32
+lib.hcr_debug_timeout_record.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]
+lib.hcr_debug_timeout_record.restype = ctypes.c_int
 lib.hcr_debug_set_variant.argtypes = [_vp, _i32]
 lib.hcr_debug_set_variant.restype = ctypes.c_int
 lib.hcr_debug_set_stall.argtypes = [_vp, _i32]
@@ -250,6 +252,13 @@ def hcr_check_device_error(handle, stream=None):
 
 def hcr_num_sms(handle) -> int:
     return lib.hcr_num_sms(handle)
+
+
+def hcr_debug_timeout_record(handle, stream=None):
+    """(status, [which wait, CTA, thread, a, b, parity]) of the first wait that gave up."""
+    out = (ctypes.c_uint32 * 6)()
+    st = lib.hcr_debug_timeout_record(handle, _stream_ptr(stream), out)
+    return st, list(out)
 
 
 def hcr_debug_set_variant(handle, variant: int) -> int:

@@ -356,8 +356,10 @@ hcr_status hcr_create(const hcr_model_dims* dims, const void* const* gamma,
   if ((ln || d.has_kv_bias) &&
       (e = cudaMalloc(&H.col_bias, sizeof(float) * 2 * d_kv * d.n_layers)) != cudaSuccess)
     return bail(e, "cudaMalloc(column bias)");
-  if ((e = cudaMalloc(&H.err, sizeof(uint32_t))) != cudaSuccess) return bail(e, "cudaMalloc(err)");
-  if ((e = cudaMemset(H.err, 0, sizeof(uint32_t))) != cudaSuccess) return bail(e, "cudaMemset");
+  if ((e = cudaMalloc(&H.err, sizeof(uint32_t) * kErrWords)) != cudaSuccess)
+    return bail(e, "cudaMalloc(err)");
+  if ((e = cudaMemset(H.err, 0, sizeof(uint32_t) * kErrWords)) != cudaSuccess)
+    return bail(e, "cudaMemset");
 
   for (int l = 0; l < d.n_layers; ++l) {
     void* dst = static_cast<uint8_t*>(H.w_packed) + size_t(per_layer) * 2 * l;
@@ -494,6 +496,17 @@ hcr_status hcr_check_device_error(hcr_handle* h, void* stream, uint32_t* flags) 
 }
 
 int32_t hcr_num_sms(const hcr_handle* h) { return h ? h->impl.num_sms : 0; }
+
+hcr_status hcr_debug_timeout_record(hcr_handle* h, void* stream, uint32_t out[6]) {
+  if (!h || !out) return fail(HCR_ERR_INVALID_ARG, "handle and out must be non-NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(out, h->impl.err + kDiagOffset, 6 * sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(h->impl.err + kDiagOffset, 0, 6 * sizeof(uint32_t));
+  if (e != cudaSuccess) return cuda_fail(e, "reading the timeout record");
+  return HCR_OK;
+}
 
 hcr_status hcr_debug_set_variant(hcr_handle* h, int32_t variant) {
   if (!h) return fail(HCR_ERR_INVALID_ARG, "handle is NULL");

@@ -36,6 +36,16 @@ constexpr size_t kProjectSmemBytes =
          : size_t(kStagesPair) * (kTileBytesA + kTileBytesB / 2)) +
     1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded pipeline waits: 2 s
+// The device error word is followed, at this word offset, by a record of the
+// first bounded wait that gave up: {which wait, CTA, thread, a, b, parity}.
+constexpr int kDiagOffset = 8;
+constexpr int kErrWords = 16;
+enum : uint32_t {
+  kWaitProducerEmpty = 1,   // a, b = tile, k-block
+  kWaitMmaAccum = 3,        // a, b = tile, accumulator
+  kWaitMmaFull = 4,         // a, b = tile, k-block
+  kWaitEpilogueAccum = 7,   // a, b = tile, accumulator
+};
 
 // tcgen05 instruction descriptor for kind::f16, fp32 accumulate, both
 // operands K-major: D format F32 (1) in bits [4,6), A and B format in

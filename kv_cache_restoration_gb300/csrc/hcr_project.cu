@@ -72,10 +72,27 @@ struct __align__(8) PipeState {
   int32_t abort;
 };
 
+// Records where a bounded wait gave up (first one wins): which wait, the CTA
+// and thread, and two call-site values (tile index, k-block or accumulator).
+__device__ __forceinline__ void record_timeout(const ProjectParams& p, uint32_t code,
+                                               uint32_t a, uint32_t b, uint32_t parity) {
+  atomicOr(p.err, uint32_t(HCR_DEVERR_TIMEOUT));
+  uint32_t* d = p.err + kDiagOffset;
+  if (atomicCAS(d, 0u, code) == 0u) {
+    d[1] = blockIdx.x;
+    d[2] = threadIdx.x;
+    d[3] = a;
+    d[4] = b;
+    d[5] = parity;
+    __threadfence();
+  }
+}
+
 // Waits for the phase of `bar` with the given parity.  Gives up when another
 // role raised the abort flag or after kWaitLimitNs, raising it itself.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int32_t* abort,
-                                           uint32_t* err) {
+                                           const ProjectParams& p, uint32_t code, uint32_t a,
+                                           uint32_t b) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
@@ -83,7 +100,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     if (*abort) return false;
     if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
       *abort = 1;
-      atomicOr(err, uint32_t(HCR_DEVERR_TIMEOUT));
+      record_timeout(p, code, a, b, parity);
       return false;
     }
   }
@@ -201,7 +218,8 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
         const int row_a = c.m * Tl::kTileM + int(rank) * kBlockM;
         const int row_b = c.n * kBlockN + int(rank) * Tl::kRowsB;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!wait_phase(ptx::smem_u32(&ps.empty[stage]), phase ^ 1u, abort, p.err)) {
+          if (!wait_phase(ptx::smem_u32(&ps.empty[stage]), phase ^ 1u, abort, p, kWaitProducerEmpty,
+                          uint32_t(tile), uint32_t(kb))) {
             ok = false;
             break;
           }
@@ -243,11 +261,14 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int64_t tile = unit; ok && tile < p.num_tiles; tile += units) {
-        if (!wait_phase(ptx::smem_u32(&ps.tempty[acc]), acc_phase ^ 1u, abort, p.err)) break;
+        if (!wait_phase(ptx::smem_u32(&ps.tempty[acc]), acc_phase ^ 1u, abort, p, kWaitMmaAccum,
+                        uint32_t(tile), uint32_t(acc)))
+          break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * kBlockN);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!wait_phase(ptx::smem_u32(&ps.full[stage]), phase, abort, p.err)) {
+          if (!wait_phase(ptx::smem_u32(&ps.full[stage]), phase, abort, p, kWaitMmaFull,
+                          uint32_t(tile), uint32_t(kb))) {
             ok = false;
             break;
           }
@@ -299,7 +320,9 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
     for (int64_t tile = unit; tile < p.num_tiles; tile += units) {
       const TileCoord c = tile_coord(tile, p);
       int ok = 0;
-      if (lane == 0) ok = wait_phase(ptx::smem_u32(&ps.tfull[acc]), acc_phase, abort, p.err);
+      if (lane == 0)
+        ok = wait_phase(ptx::smem_u32(&ps.tfull[acc]), acc_phase, abort, p, kWaitEpilogueAccum,
+                        uint32_t(tile), uint32_t(acc));
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();

@@ -25,6 +25,13 @@ def test_stalled_pipeline_times_out_and_context_survives(cuda_device, variant):
     assert case.status == B.HCR_ERR_TIMEOUT
     assert case.flags & B.HCR_DEVERR_TIMEOUT
     assert 1.5 < elapsed < 60.0
+    # the record names the first wait that gave up: the MMA's wait for the
+    # stage whose load was withheld (k-block 0), or the epilogue's wait for
+    # that tile's accumulator (accumulator 0), on one of the 4 tiles
+    st, rec = B.hcr_debug_timeout_record(case.restorer.handle)
+    assert st == B.HCR_OK
+    assert rec[0] in (4, 7) and rec[3] < 4 and rec[4] == 0, rec
+    assert B.hcr_debug_timeout_record(case.restorer.handle)[1][0] == 0   # cleared
     assert B.hcr_debug_set_stall(case.restorer.handle, False) == B.HCR_OK
     again = Hn.run(Hn.make_case(w, cuda_device, params=case.params, restorer=case.restorer))
     assert again.status == 0

@@ -35,6 +35,17 @@ SMALL_CASES = [
     W("block1", ModelShape("b1", 1, 256, 2, 2, 64), [40, 9], [3, 0], block_size=1,
       block_order="shuffled"),
     W("theta5e5", ModelShape("t5", 1, 256, 2, 2, 128, rope_theta=5e5), [64], [20000]),
+    W("fp16-rope", ModelShape("f16r", 2, 384, 3, 3, 128, dtype="fp16"), [200, 57], [11, 300],
+      block_order="shuffled"),
+    W("many-requests", ModelShape("mr", 1, 256, 2, 2, 64),
+      [int(x) for x in np.random.default_rng(3).integers(0, 21, 150)],
+      [int(x) for x in np.random.default_rng(4).integers(0, 200, 150)], block_size=32,
+      block_order="shuffled"),
+    W("single-token", ModelShape("one", 2, 256, 2, 2, 128), [1], [77]),
+    W("ln-dh256", ModelShape("ln256", 1, 512, 2, 2, 256, norm="ln", kv_bias=True), [260], [3]),
+    W("d8192", ModelShape("d8k", 1, 8192, 2, 2, 128), [300], [0]),
+    W("block64", ModelShape("b64", 1, 256, 4, 4, 64), [333, 2], [65, 0], block_size=64,
+      block_order="shuffled"),
 ]
 
 

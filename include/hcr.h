@@ -29,10 +29,13 @@
  * (W' = [W_k; W_v] diag(gamma), rounded once to the storage type), so the
  * norm is applied as a per-row scale after the GEMM.
  *
- * Threading and streams: a handle is immutable after hcr_create and may be
- * used from several host threads and streams at once, provided each
- * concurrent restore has its own workspace.  Every call that takes a stream
- * only enqueues work on it; it does not synchronise unless stated.
+ * Threading and streams: a handle is immutable after hcr_create (apart from
+ * the hcr_debug_* testing hooks) and may be used from several host threads
+ * and streams at once, provided each concurrent restore has its own
+ * workspace.  The handle's device error word is shared: bits raised by any
+ * of its restores are reported (and cleared) by the next
+ * hcr_check_device_error.  Every call that takes a stream only enqueues work
+ * on it; it does not synchronise unless stated.
  *
  * All entry points return hcr_status.  Host-side argument errors are
  * reported before any work is enqueued, and hcr_last_error() then returns a

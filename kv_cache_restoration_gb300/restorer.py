@@ -57,8 +57,28 @@ class Restorer:
             self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
         return self._ws
 
+    def _check_tensors(self, hidden, cu_seqlens, start_pos, block_table, k_cache, v_cache):
+        """The library reads raw pointers: shapes are the caller's contract, but
+        layout, dtype and device mistakes are caught here."""
+        dt = self.torch_dtype
+        for name, t, want in (("hidden", hidden, dt), ("k_cache", k_cache, dt),
+                              ("v_cache", v_cache, dt), ("cu_seqlens", cu_seqlens, torch.int32),
+                              ("start_pos", start_pos, torch.int32),
+                              ("block_table", block_table, torch.int32)):
+            if not isinstance(t, torch.Tensor):
+                raise TypeError(f"{name} must be a torch.Tensor")
+            if not t.is_cuda:
+                raise ValueError(f"{name} must be on a CUDA device")
+            if t.dtype != want:
+                raise TypeError(f"{name} must be {want}, got {t.dtype}")
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+        if hidden.dim() != 3 or hidden.shape[-1] != self.dims.d_model:
+            raise ValueError(f"hidden must be [layers][tokens][{self.dims.d_model}]")
+
     def _args(self, hidden, layer_begin, layer_end, cu_seqlens, start_pos, block_table,
               k_cache, v_cache, num_blocks, block_size, layer_stride_elems, workspace):
+        self._check_tensors(hidden, cu_seqlens, start_pos, block_table, k_cache, v_cache)
         n_req = int(start_pos.numel())
         n_tokens = int(hidden.shape[-2]) if hidden is not None and hidden.dim() >= 2 else 0
         nl = layer_end - layer_begin

@@ -20,8 +20,8 @@ constexpr int kBlockN = 256;           // K||V columns per tile (TMEM columns pe
 constexpr int kBlockK = 64;            // 64 x 2 bytes = one 128-byte swizzle row
 constexpr int kUmmaK = 16;             // K of one tcgen05.mma kind::f16
 constexpr int kStages = 4;             // TMA -> MMA ring depth, single-CTA variant (48 KB stages)
-constexpr int kStagesPair = 6;         // ring depth per CTA, CTA-pair variant (32 KB stages)
-constexpr int kStagesMax = 6;
+constexpr int kStagesPair = 7;         // ring depth per CTA, CTA-pair variant (32 KB stages)
+constexpr int kStagesMax = 7;
 constexpr int kAccums = 2;             // TMEM accumulators (epilogue overlaps next mainloop)
 constexpr int kTileBytesA = kBlockM * kBlockK * 2;
 constexpr int kTileBytesB = kBlockN * kBlockK * 2;
@@ -29,12 +29,11 @@ constexpr int kStageBytes = kTileBytesA + kTileBytesB;
 constexpr int kProjectThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kEpilogueWarps = 4;
 constexpr int kGroupM = 16;            // m-tiles per raster group (L2 reuse of hidden rows)
-// dynamic shared memory of either variant (both rings are 192 KB) + alignment slack
-constexpr size_t kProjectSmemBytes =
-    (size_t(kStages) * kStageBytes > size_t(kStagesPair) * (kTileBytesA + kTileBytesB / 2)
-         ? size_t(kStages) * kStageBytes
-         : size_t(kStagesPair) * (kTileBytesA + kTileBytesB / 2)) +
-    1024;
+// dynamic shared memory of each variant's ring + slack to align it to 1024 bytes
+constexpr size_t kSmemSingle = size_t(kStages) * kStageBytes + 1024;
+constexpr size_t kSmemPair = size_t(kStagesPair) * (kTileBytesA + kTileBytesB / 2) + 1024;
+static_assert(kSmemSingle <= 232448 - 512 && kSmemPair <= 232448 - 512,
+              "ring does not fit the 227 KB of shared memory a CTA can use");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded pipeline waits: 2 s
 // The device error word is followed, at this word offset, by a record of the
 // first bounded wait that gave up: {which wait, CTA, thread, a, b, parity}.

@@ -25,7 +25,7 @@
 //               owns one 32-lane TMEM quadrant = 32 tokens), overlapping the
 //               MMA of the next tile into the other accumulator.
 // Two variants: single CTAs with 128x256 tiles (cta_group::1, 4 stages of
-// 48 KB), and CTA pairs with 256x256 tiles (cta_group::2, 6 stages of 32 KB
+// 48 KB), and CTA pairs with 256x256 tiles (cta_group::2, 7 stages of 32 KB
 // per CTA).  The pair halves each SM's share of the weight tile, which cuts
 // shared-memory traffic per MMA by a third; the host picks the pair for
 // restores of more than 128 tokens.
@@ -143,7 +143,7 @@ __device__ __forceinline__ void store16(uint16_t* dst, const float (&x)[16]) {
 // Per-variant tiling.  Single: one CTA computes a 128x256 tile with
 // cta_group::1.  Pair: a cluster of two CTAs computes a 256x256 tile with one
 // cta_group::2 MMA stream; each CTA stages its own 128 rows of A and half of
-// B (128 rows), so a stage is 32 KB instead of 48 KB and six fit.
+// B (128 rows), so a stage is 32 KB instead of 48 KB and seven fit.
 template <bool PAIR>
 struct Tiling {
   static constexpr int kStages = PAIR ? ::hcr::kStagesPair : ::hcr::kStages;
@@ -456,13 +456,14 @@ template <int DT, bool PAIR>
 cudaError_t launch_variant(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
                            const ProjectParams& p, int grid, cudaStream_t s) {
   auto kernel = project_kernel<DT, PAIR>;
+  constexpr size_t smem = PAIR ? kSmemPair : kSmemSingle;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(kProjectSmemBytes));
+                                       int(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid));
   cfg.blockDim = dim3(kProjectThreads);
-  cfg.dynamicSmemBytes = kProjectSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   if (PAIR) {
@@ -480,7 +481,7 @@ template <int DT>
 int max_pair_clusters() {
   auto kernel = project_kernel<DT, true>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(kProjectSmemBytes)) != cudaSuccess)
+                           int(kSmemPair)) != cudaSuccess)
     return -1;
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
@@ -488,7 +489,7 @@ int max_pair_clusters() {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(sms & ~1));
   cfg.blockDim = dim3(kProjectThreads);
-  cfg.dynamicSmemBytes = kProjectSmemBytes;
+  cfg.dynamicSmemBytes = kSmemPair;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;

@@ -210,6 +210,11 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmap_h);
       ptx::tma_prefetch_desc(&tmap_w);
+      // A weight tile is read by every m-tile of its raster group: with several
+      // m-tiles keep it in L2 ahead of other data (with one it is streamed
+      // once and loaded without a hint).
+      const bool reuse_w = p.m_tiles > 1;
+      const uint64_t keep = ptx::policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -233,14 +238,22 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
             const uint32_t full_leader = ptx::mapa_shared(full, 0);
             if (!(p.debug_stall && issued == 0)) {
               ptx::tma_load_3d_pair(dst_a, &tmap_h, full_leader, kb * kBlockK, row_a, c.l);
-              ptx::tma_load_3d_pair(dst_b, &tmap_w, full_leader, kb * kBlockK, row_b,
-                                    p.layer_begin + c.l);
+              if (reuse_w)
+                ptx::tma_load_3d_pair_hint(dst_b, &tmap_w, full_leader, kb * kBlockK, row_b,
+                                           p.layer_begin + c.l, keep);
+              else
+                ptx::tma_load_3d_pair(dst_b, &tmap_w, full_leader, kb * kBlockK, row_b,
+                                      p.layer_begin + c.l);
             }
           } else {
             ptx::mbar_arrive_expect_tx(full, Tl::kStageBytes);
             if (!(p.debug_stall && issued == 0)) {
               ptx::tma_load_3d(dst_a, &tmap_h, full, kb * kBlockK, row_a, c.l);
-              ptx::tma_load_3d(dst_b, &tmap_w, full, kb * kBlockK, row_b, p.layer_begin + c.l);
+              if (reuse_w)
+                ptx::tma_load_3d_hint(dst_b, &tmap_w, full, kb * kBlockK, row_b,
+                                      p.layer_begin + c.l, keep);
+              else
+                ptx::tma_load_3d(dst_b, &tmap_w, full, kb * kBlockK, row_b, p.layer_begin + c.l);
             }
           }
           ++issued;

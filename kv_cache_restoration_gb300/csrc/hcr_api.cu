@@ -17,13 +17,18 @@ namespace {
 
 thread_local std::string g_last_error;
 
-hcr_status fail(hcr_status s, const char* fmt, ...) {
+hcr_status vrecord(hcr_status s, const char* fmt, va_list ap) {
   char buf[512];
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  g_last_error = buf;
+  return s;
+}
+
+hcr_status fail(hcr_status s, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
-  vsnprintf(buf, sizeof buf, fmt, ap);
+  vrecord(s, fmt, ap);
   va_end(ap);
-  g_last_error = buf;
   return s;
 }
 
@@ -268,12 +273,10 @@ void free_handle(Handle& H) {
 }  // namespace
 
 hcr_status set_last_error(hcr_status s, const char* fmt, ...) {
-  char buf[512];
   va_list ap;
   va_start(ap, fmt);
-  vsnprintf(buf, sizeof buf, fmt, ap);
+  vrecord(s, fmt, ap);
   va_end(ap);
-  g_last_error = buf;
   return s;
 }
 

@@ -290,6 +290,27 @@ def gpu_arm(args, rank, world, local_rank):
     staging = torch.empty(args.e2e_slots * chunk_bytes, dtype=torch.uint8, device=device)
     layout = B.hcr_cache_layout(lay.num_blocks, lay.block_size, 0)
     e2e_steps = min(args.steps, args.e2e_steps)
+    src = None
+    if args.e2e_source == "chunks" and e2e_steps > 0:
+        # The saved form: 64-token chunks [chunk][layer][row][d] in pinned host
+        # memory, written once by the save kernel before the timed region.
+        import dataclasses
+        import numpy as np
+        clay = G.request_layout(dataclasses.replace(w, block_size=args.e2e_chunk_tokens))
+        ctab_np = np.ascontiguousarray(clay.block_table, dtype=np.int32)
+        store = torch.empty((clay.num_blocks, L, args.e2e_chunk_tokens, s.d_model),
+                            dtype=case.hidden.dtype).pin_memory()
+        ctab = torch.as_tensor(ctab_np, device=device)
+        B.hcr_save_hidden(r.handle, case.hidden, 0, L, w.n_req, T, case.cu, case.start, ctab,
+                          int(ctab.shape[1]), args.e2e_chunk_tokens, store, clay.num_blocks,
+                          stream)
+        torch.cuda.synchronize(device)
+        cu_np = np.ascontiguousarray(lay.cu_seqlens, dtype=np.int32)
+        start_np = np.ascontiguousarray(lay.start_pos, dtype=np.int32)
+        src = B.hcr_chunk_source(store.data_ptr(), args.e2e_chunk_tokens, clay.num_blocks,
+                                 ctab_np.ctypes.data, int(ctab_np.shape[1]), cu_np.ctypes.data,
+                                 start_np.ctypes.data)
+        src._keep = (store, ctab_np, cu_np, start_np)
     t0 = time.perf_counter()
     for i in range(2 + e2e_steps if e2e_steps > 0 else 0):
         if i == 2:
@@ -297,9 +318,16 @@ def gpu_arm(args, rank, world, local_rank):
             t0 = time.perf_counter()
         for hm, dm in zip(meta_host, meta_dev):
             dm.copy_(hm, non_blocking=True)
-        B.hcr_restore_streamed(r.handle, hidden_host, 0, L, w.n_req, T, case.cu, case.start,
-                               case.table, lay.max_blocks, case.k_cache, case.v_cache, layout,
-                               staging, staging.numel(), chunk, ws, ws.numel(), stream)
+        if src is None:
+            B.hcr_restore_streamed(r.handle, hidden_host, 0, L, w.n_req, T, case.cu,
+                                   case.start, case.table, lay.max_blocks, case.k_cache,
+                                   case.v_cache, layout, staging, staging.numel(), chunk, ws,
+                                   ws.numel(), stream)
+        else:
+            B.hcr_restore_streamed_chunks(r.handle, src, 0, L, w.n_req, T, case.cu, case.start,
+                                          case.table, lay.max_blocks, case.k_cache,
+                                          case.v_cache, layout, staging, staging.numel(), chunk,
+                                          ws, ws.numel(), stream)
         st, _ = r.check(stream)          # syncs and reads the 4-byte status word
         if st != 0:
             raise RuntimeError("device error in e2e leg")
@@ -424,6 +452,10 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=30, help="0 skips the end-to-end leg")
     ap.add_argument("--e2e-chunk", type=int, default=4, help="layers per streamed chunk")
     ap.add_argument("--e2e-slots", type=int, default=3, help="staging ring slots")
+    ap.add_argument("--e2e-source", default="layers", choices=["layers", "chunks"],
+                    help="host form of the hidden states: [layer][token][d], or the saved "
+                         "chunk store")
+    ap.add_argument("--e2e-chunk-tokens", type=int, default=64, help="tokens per saved chunk")
     ap.add_argument("--variant", type=int, default=0,
                     help="project kernel tiles: 0 automatic, 1 single CTAs, 2 CTA pairs")
     ap.add_argument("--layers", type=int, default=0,
@@ -544,8 +576,11 @@ def main():
                  "unit": "tokens/s",
                  "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": 4,
                  "ms_per_step": res["e2e_s"] * 1e3,
-                 "api": f"hcr_restore_streamed, {res['chunk']}-layer chunks, "
-                        f"{args.e2e_slots}-slot staging ring",
+                 "api": (f"hcr_restore_streamed, {res['chunk']}-layer chunks, "
+                         if args.e2e_source == "layers" else
+                         f"hcr_restore_streamed_chunks from a pinned host store of "
+                         f"{args.e2e_chunk_tokens}-token chunks, {res['chunk']}-layer groups, ")
+                        + f"{args.e2e_slots}-slot staging ring",
                  "plain_h2d_gbs": res["h2d_gbs"]}
                 if res["e2e_s"] == res["e2e_s"] else None),
         "gpu_launches": res["launches"],

@@ -262,6 +262,41 @@ hcr_status hcr_save_hidden(hcr_handle* h, const void* hidden, int32_t layer_begi
                            void* stream);
 
 /*
+ * hcr_restore_streamed_chunks -- hcr_restore_streamed from a host store of
+ * fixed-size chunks, in the layout hcr_save_hidden writes:
+ *     store[chunk][layer][row][d_model],  chunk = chunk_table[r][pos / C],
+ *     row = pos % C.
+ * This is the restore half of the HCache episode's storage scheme (cue 22:
+ * 64-token chunks).  The copy engines gather each request's rows straight
+ * from the chunks into the staging ring with 2-D copies (one per run of a
+ * request's tokens inside one chunk, per chunk of layers), so no host-side
+ * transpose is needed.  The host needs the request layout to plan those
+ * copies, so it is given in host memory here (the device copies in the
+ * argument list are still used by the kernels).  Every other argument and
+ * all behaviour are as in hcr_restore_streamed.  Host-side checks reject a
+ * position without a chunk or a chunk id outside [0, num_chunks).
+ */
+typedef struct {
+  const void* store;           /* HOST (pinned) [num_chunks][n_layers][chunk_tokens][d_model] */
+  int32_t chunk_tokens;        /* C: tokens per chunk (64 on the page)                         */
+  int32_t num_chunks;
+  const int32_t* chunk_table;  /* HOST [n_req][max_chunks]                                     */
+  int32_t max_chunks;
+  const int32_t* cu_seqlens;   /* HOST [n_req+1], same values as the device copy              */
+  const int32_t* start_pos;    /* HOST [n_req], same values as the device copy                */
+} hcr_chunk_source;
+
+hcr_status hcr_restore_streamed_chunks(hcr_handle* h, const hcr_chunk_source* source,
+                                       int32_t layer_begin, int32_t layer_end, int32_t n_req,
+                                       int32_t n_tokens, const int32_t* cu_seqlens,
+                                       const int32_t* start_pos, const int32_t* block_table,
+                                       int32_t max_blocks_per_req, void* k_cache,
+                                       void* v_cache, const hcr_cache_layout* layout,
+                                       void* staging, size_t staging_bytes,
+                                       int32_t layers_per_chunk, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+/*
  * hcr_restore_no_alloc -- hcr_restore without a caller-provided workspace.
  *
  * The paper has no counterpart to this call; it exists for callers of this

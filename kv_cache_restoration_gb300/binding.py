@@ -47,6 +47,13 @@ class hcr_cache_layout(ctypes.Structure):
                 ("layer_stride_elems", ctypes.c_int64)]
 
 
+class hcr_chunk_source(ctypes.Structure):
+    _fields_ = [("store", ctypes.c_void_p), ("chunk_tokens", ctypes.c_int32),
+                ("num_chunks", ctypes.c_int32), ("chunk_table", ctypes.c_void_p),
+                ("max_chunks", ctypes.c_int32), ("cu_seqlens", ctypes.c_void_p),
+                ("start_pos", ctypes.c_void_p)]
+
+
 class HcrError(RuntimeError):
     def __init__(self, status: int, where: str, message: str):
         super().__init__(f"{where}: {message}")
@@ -84,6 +91,9 @@ lib.hcr_restore_streamed.restype = ctypes.c_int
 lib.hcr_save_hidden.argtypes = [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _vp,
                                 _i32, _vp]
 lib.hcr_save_hidden.restype = ctypes.c_int
+lib.hcr_restore_streamed_chunks.argtypes = [_vp, ctypes.POINTER(hcr_chunk_source)] + \
+    _RESTORE_ARGTYPES[2:13] + [_vp, ctypes.c_size_t, _i32, _vp, ctypes.c_size_t, _vp]
+lib.hcr_restore_streamed_chunks.restype = ctypes.c_int
 lib.hcr_restore_no_alloc.argtypes = _RESTORE_ARGTYPES[:13] + [_vp]
 lib.hcr_restore_no_alloc.restype = ctypes.c_int
 HCR_NO_ALLOC_SCRATCH_BYTES = 16 << 20
@@ -213,6 +223,22 @@ def hcr_restore_streamed(handle, hidden_host, layer_begin, layer_end, n_req, n_t
         layers_per_chunk, _ptr(workspace), workspace_bytes, _stream_ptr(stream))
     if check:
         _check(st, "hcr_restore_streamed")
+    return st
+
+
+def hcr_restore_streamed_chunks(handle, source: hcr_chunk_source, layer_begin, layer_end, n_req,
+                                n_tokens, cu_seqlens, start_pos, block_table, max_blocks_per_req,
+                                k_cache, v_cache, layout, staging, staging_bytes,
+                                layers_per_chunk, workspace, workspace_bytes, stream=None, *,
+                                check: bool = True) -> int:
+    """Layer-pipelined restore from a host chunk store (hcr_save_hidden's layout)."""
+    st = lib.hcr_restore_streamed_chunks(
+        handle, ctypes.byref(source), layer_begin, layer_end, n_req, n_tokens, _ptr(cu_seqlens),
+        _ptr(start_pos), _ptr(block_table), max_blocks_per_req, _ptr(k_cache), _ptr(v_cache),
+        ctypes.byref(layout) if layout is not None else None, _ptr(staging), staging_bytes,
+        layers_per_chunk, _ptr(workspace), workspace_bytes, _stream_ptr(stream))
+    if check:
+        _check(st, "hcr_restore_streamed_chunks")
     return st
 
 

@@ -12,7 +12,16 @@
 //
 //   copy stream:   [copy c0][copy c1][copy c2]....          (waits done[slot])
 //   caller stream:          [restore c0][restore c1][....   (waits copied[slot])
+//
+// The host copy is either [layer][token][d] hidden states (one linear copy
+// per chunk of layers) or a store of fixed-size chunks as hcr_save_hidden
+// writes them ([chunk][layer][row][d]): then every run of one request's
+// tokens inside one chunk becomes one 2-D copy that gathers its rows for all
+// layers of the chunk of layers at once, so the copy engines do the
+// chunk-to-layer transpose on the way.
+#include <functional>
 #include <mutex>
+#include <vector>
 
 #include "hcr_internal.h"
 
@@ -66,25 +75,18 @@ hcr_status ensure_resources(Handle& H, StreamedRes** out) {
   return HCR_OK;
 }
 
-}  // namespace
-}  // namespace hcr
+// Copies the hidden states of layers [l0, l0 + nl) (relative to the restore's
+// first layer) into `dst` laid out [nl][n_tokens][d_model], on `copy`.
+using CopyFn = std::function<cudaError_t(void* dst, int32_t l0, int32_t nl, cudaStream_t copy)>;
 
-using namespace hcr;
-
-extern "C" hcr_status hcr_restore_streamed(
-    hcr_handle* h, const void* hidden_host, int32_t layer_begin, int32_t layer_end,
-    int32_t n_req, int32_t n_tokens, const int32_t* cu_seqlens, const int32_t* start_pos,
-    const int32_t* block_table, int32_t max_blocks_per_req, void* k_cache, void* v_cache,
-    const hcr_cache_layout* layout, void* staging, size_t staging_bytes,
-    int32_t layers_per_chunk, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!h) return set_last_error(HCR_ERR_INVALID_ARG, "handle is NULL");
+hcr_status streamed_pipeline(hcr_handle* h, int32_t layer_begin, int32_t layer_end,
+                             int32_t n_req, int32_t n_tokens, const int32_t* cu_seqlens,
+                             const int32_t* start_pos, const int32_t* block_table,
+                             int32_t max_blocks_per_req, void* k_cache, void* v_cache,
+                             const hcr_cache_layout* layout, void* staging, size_t staging_bytes,
+                             int32_t layers_per_chunk, void* workspace, size_t workspace_bytes,
+                             void* stream, const CopyFn& copy_layers) {
   const hcr_model_dims& d = h->impl.dims;
-  if (layer_begin < 0 || layer_end < layer_begin || layer_end > d.n_layers)
-    return set_last_error(HCR_ERR_INVALID_ARG, "layer range [%d, %d) outside [0, %d)",
-                          layer_begin, layer_end, d.n_layers);
-  if (n_tokens < 0) return set_last_error(HCR_ERR_INVALID_ARG, "n_tokens must be >= 0");
-  if (n_tokens == 0 || layer_end == layer_begin) return HCR_OK;
-  if (!hidden_host) return set_last_error(HCR_ERR_INVALID_ARG, "hidden_host is NULL");
   if (!layout) return set_last_error(HCR_ERR_INVALID_ARG, "layout is NULL");
   if (layers_per_chunk < 1)
     return set_last_error(HCR_ERR_INVALID_ARG, "layers_per_chunk must be >= 1");
@@ -121,7 +123,6 @@ extern "C" hcr_status hcr_restore_streamed(
   if ((e = cudaEventRecord(r->start, s)) != cudaSuccess) return cuda_err(e, "event record");
   if ((e = cudaStreamWaitEvent(r->copy, r->start, 0)) != cudaSuccess)
     return cuda_err(e, "stream wait");
-  const uint8_t* src = static_cast<const uint8_t*>(hidden_host);
   uint8_t* ring = static_cast<uint8_t*>(staging);
   int c = 0;
   for (int32_t l0 = 0; l0 < n_layers; l0 += chunk, ++c) {
@@ -130,8 +131,7 @@ extern "C" hcr_status hcr_restore_streamed(
     void* dst = ring + size_t(slot) * chunk_bytes;
     if (c >= slots && (e = cudaStreamWaitEvent(r->copy, r->done[slot], 0)) != cudaSuccess)
       return cuda_err(e, "stream wait");
-    if ((e = cudaMemcpyAsync(dst, src + size_t(l0) * layer_bytes, size_t(nl) * layer_bytes,
-                             cudaMemcpyHostToDevice, r->copy)) != cudaSuccess)
+    if ((e = copy_layers(dst, l0, nl, r->copy)) != cudaSuccess)
       return cuda_err(e, "hidden-state copy");
     if ((e = cudaEventRecord(r->copied[slot], r->copy)) != cudaSuccess)
       return cuda_err(e, "event record");
@@ -147,4 +147,137 @@ extern "C" hcr_status hcr_restore_streamed(
       return cuda_err(e, "event record");
   }
   return HCR_OK;
+}
+
+}  // namespace
+}  // namespace hcr
+
+using namespace hcr;
+
+extern "C" hcr_status hcr_restore_streamed(
+    hcr_handle* h, const void* hidden_host, int32_t layer_begin, int32_t layer_end,
+    int32_t n_req, int32_t n_tokens, const int32_t* cu_seqlens, const int32_t* start_pos,
+    const int32_t* block_table, int32_t max_blocks_per_req, void* k_cache, void* v_cache,
+    const hcr_cache_layout* layout, void* staging, size_t staging_bytes,
+    int32_t layers_per_chunk, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!h) return set_last_error(HCR_ERR_INVALID_ARG, "handle is NULL");
+  const hcr_model_dims& d = h->impl.dims;
+  if (layer_begin < 0 || layer_end < layer_begin || layer_end > d.n_layers)
+    return set_last_error(HCR_ERR_INVALID_ARG, "layer range [%d, %d) outside [0, %d)",
+                          layer_begin, layer_end, d.n_layers);
+  if (n_tokens < 0) return set_last_error(HCR_ERR_INVALID_ARG, "n_tokens must be >= 0");
+  if (n_tokens == 0 || layer_end == layer_begin) return HCR_OK;
+  if (!hidden_host) return set_last_error(HCR_ERR_INVALID_ARG, "hidden_host is NULL");
+  const uint8_t* src = static_cast<const uint8_t*>(hidden_host);
+  const size_t layer_bytes = size_t(n_tokens) * size_t(d.d_model) * 2;
+  return streamed_pipeline(
+      h, layer_begin, layer_end, n_req, n_tokens, cu_seqlens, start_pos, block_table,
+      max_blocks_per_req, k_cache, v_cache, layout, staging, staging_bytes, layers_per_chunk,
+      workspace, workspace_bytes, stream,
+      [&](void* dst, int32_t l0, int32_t nl, cudaStream_t copy) {
+        return cudaMemcpyAsync(dst, src + size_t(l0) * layer_bytes, size_t(nl) * layer_bytes,
+                               cudaMemcpyHostToDevice, copy);
+      });
+}
+
+extern "C" hcr_status hcr_restore_streamed_chunks(
+    hcr_handle* h, const hcr_chunk_source* source, int32_t layer_begin, int32_t layer_end,
+    int32_t n_req, int32_t n_tokens, const int32_t* cu_seqlens, const int32_t* start_pos,
+    const int32_t* block_table, int32_t max_blocks_per_req, void* k_cache, void* v_cache,
+    const hcr_cache_layout* layout, void* staging, size_t staging_bytes,
+    int32_t layers_per_chunk, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!h) return set_last_error(HCR_ERR_INVALID_ARG, "handle is NULL");
+  const hcr_model_dims& d = h->impl.dims;
+  if (layer_begin < 0 || layer_end < layer_begin || layer_end > d.n_layers)
+    return set_last_error(HCR_ERR_INVALID_ARG, "layer range [%d, %d) outside [0, %d)",
+                          layer_begin, layer_end, d.n_layers);
+  if (n_tokens < 0 || n_req < 0)
+    return set_last_error(HCR_ERR_INVALID_ARG, "n_tokens and n_req must be >= 0");
+  if (n_tokens == 0 || layer_end == layer_begin) return HCR_OK;
+  if (!source || !source->store || !source->chunk_table || !source->cu_seqlens ||
+      !source->start_pos)
+    return set_last_error(HCR_ERR_INVALID_ARG, "source and its host arrays must be non-NULL");
+  const hcr_chunk_source& src = *source;
+  if (src.chunk_tokens < 1 || src.num_chunks < 1 || src.max_chunks < 1)
+    return set_last_error(HCR_ERR_INVALID_ARG,
+                          "chunk_tokens, num_chunks and max_chunks must be >= 1");
+  if (src.cu_seqlens[0] != 0 || src.cu_seqlens[n_req] != n_tokens)
+    return set_last_error(HCR_ERR_INVALID_ARG, "host cu_seqlens must run from 0 to n_tokens");
+
+  // Plan the gathers once.  A run is one request's tokens inside one chunk;
+  // its rows for nl consecutive layers sit C*d elements apart in the chunk and
+  // n_tokens*d apart in the staging slot, so one 2-D copy moves them all.  A
+  // span is a run of whole chunks with consecutive ids: for one layer its
+  // chunks sit n_layers*C*d apart in the store and land C*d apart, so one 2-D
+  // copy per layer moves the whole span -- fewer copies when the span holds
+  // more chunks than the group has layers.
+  struct Run {
+    size_t src_off;     // bytes into the store: (first chunk, layer_begin, first row)
+    size_t dst_off;     // bytes into a staging slot: (layer 0, first token)
+    size_t width;       // bytes per chunk: rows x d_model x 2
+    int64_t n_chunks;   // whole consecutive chunks in a span; 0 for a partial run
+  };
+  std::vector<Run> runs;
+  const int64_t C = src.chunk_tokens;
+  const size_t row_bytes = size_t(d.d_model) * 2;
+  const size_t chunk_stride = size_t(d.n_layers) * size_t(C) * row_bytes;   // next chunk id
+  int32_t prev_cid = -1;
+  for (int32_t r = 0; r < n_req; ++r) {
+    const int32_t a = src.cu_seqlens[r], b = src.cu_seqlens[r + 1];
+    if (b < a) return set_last_error(HCR_ERR_INVALID_ARG, "host cu_seqlens must not decrease");
+    const int64_t p0 = src.start_pos[r];
+    if (p0 < 0) return set_last_error(HCR_ERR_INVALID_ARG, "request %d: negative start", r);
+    bool span_open = false;
+    for (int64_t p = p0; p < p0 + (b - a);) {
+      const int64_t k = p / C, off = p % C;
+      const int64_t rows = std::min<int64_t>(C - off, p0 + (b - a) - p);
+      if (k >= src.max_chunks)
+        return set_last_error(HCR_ERR_INVALID_ARG, "request %d: position %lld has no chunk", r,
+                              (long long)p);
+      const int32_t cid = src.chunk_table[int64_t(r) * src.max_chunks + k];
+      if (cid < 0 || cid >= src.num_chunks)
+        return set_last_error(HCR_ERR_INVALID_ARG, "request %d: chunk id %d out of range", r,
+                              cid);
+      const int64_t t = a + (p - p0);
+      const bool whole = rows == C;
+      if (whole && span_open && cid == prev_cid + 1) {
+        ++runs.back().n_chunks;
+      } else {
+        runs.push_back({((size_t(cid) * d.n_layers + layer_begin) * C + off) * row_bytes,
+                        size_t(t) * row_bytes, size_t(rows) * row_bytes, whole ? 1 : 0});
+      }
+      span_open = whole;
+      prev_cid = cid;
+      p += rows;
+    }
+  }
+  const uint8_t* store = static_cast<const uint8_t*>(src.store);
+  const size_t layer_in_chunk = size_t(C) * row_bytes;       // next layer inside a chunk
+  const size_t layer_in_slot = size_t(n_tokens) * row_bytes;  // next layer in the slot
+  return streamed_pipeline(
+      h, layer_begin, layer_end, n_req, n_tokens, cu_seqlens, start_pos, block_table,
+      max_blocks_per_req, k_cache, v_cache, layout, staging, staging_bytes, layers_per_chunk,
+      workspace, workspace_bytes, stream,
+      [&](void* dst, int32_t l0, int32_t nl, cudaStream_t copy) {
+        uint8_t* slot = static_cast<uint8_t*>(dst);
+        cudaError_t e = cudaSuccess;
+        for (const Run& run : runs) {
+          const uint8_t* base = store + run.src_off + size_t(l0) * layer_in_chunk;
+          if (run.n_chunks > nl) {
+            for (int32_t l = 0; l < nl && e == cudaSuccess; ++l)
+              e = cudaMemcpy2DAsync(slot + size_t(l) * layer_in_slot + run.dst_off,
+                                    layer_in_chunk, base + size_t(l) * layer_in_chunk,
+                                    chunk_stride, run.width, size_t(run.n_chunks),
+                                    cudaMemcpyHostToDevice, copy);
+          } else {
+            for (int64_t j = 0; j < std::max<int64_t>(run.n_chunks, 1) && e == cudaSuccess; ++j)
+              e = cudaMemcpy2DAsync(slot + run.dst_off + size_t(j) * layer_in_chunk,
+                                    layer_in_slot, base + size_t(j) * chunk_stride,
+                                    layer_in_chunk, run.width, size_t(nl),
+                                    cudaMemcpyHostToDevice, copy);
+          }
+          if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+      });
 }

@@ -297,6 +297,101 @@ hcr_status hcr_restore_streamed_chunks(hcr_handle* h, const hcr_chunk_source* so
                                        size_t workspace_bytes, void* stream);
 
 /*
+ * hcr_save_kv / hcr_load_kv -- the KV-offload side of a layer-split restore
+ * (HCache episode, cue 18: layers not restored from hidden states are handed
+ * to a complementary method; the one provided here is KV offload).
+ *
+ * A dense K/V store holds, for layers [layer_begin, layer_end) and the
+ * n_tokens tokens of the request layout (cu_seqlens order):
+ *     kv[layer - layer_begin][0][t][:] = K row of token t (position-embedded)
+ *     kv[layer - layer_begin][1][t][:] = V row of token t
+ * each row n_kv_heads * head_dim elements of the storage dtype.
+ * hcr_save_kv copies those rows out of the paged cache (e.g. when a
+ * request's cache is evicted); hcr_load_kv places them back, at the slots the
+ * block table gives -- the same placement hcr_restore uses.  `kv` may be
+ * device memory or pinned (mapped) host memory; it must be 16-byte aligned.
+ * Other arguments are as in hcr_restore; the workspace needs
+ * hcr_workspace_bytes(h, n_tokens, 1) bytes (only the slot map is built).
+ * Rows whose placement is invalid are skipped and flagged as in hcr_restore.
+ * Each call enqueues two kernels on `stream`.
+ */
+hcr_status hcr_load_kv(hcr_handle* h, const void* kv, int32_t layer_begin, int32_t layer_end,
+                       int32_t n_req, int32_t n_tokens, const int32_t* cu_seqlens,
+                       const int32_t* start_pos, const int32_t* block_table,
+                       int32_t max_blocks_per_req, void* k_cache, void* v_cache,
+                       const hcr_cache_layout* layout, void* workspace, size_t workspace_bytes,
+                       void* stream);
+hcr_status hcr_save_kv(hcr_handle* h, void* kv, int32_t layer_begin, int32_t layer_end,
+                       int32_t n_req, int32_t n_tokens, const int32_t* cu_seqlens,
+                       const int32_t* start_pos, const int32_t* block_table,
+                       int32_t max_blocks_per_req, const void* k_cache, const void* v_cache,
+                       const hcr_cache_layout* layout, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/*
+ * The bubble-free layer split (HCache episode, cue 18; cue 20 on splitting by
+ * layer rather than by token).  A restore of L layers pipelines host-to-device
+ * transfer against GPU work; whichever is slower sets the pace.  Restoring a
+ * layer from hidden states costs hidden_copy_s of transfer and restore_s of
+ * GPU time; loading it as saved K/V costs kv_copy_s and kv_place_s.
+ * hcr_plan_layer_split returns the split with the smallest
+ *     max(transfer, compute),  transfer = (L-k)*hidden_copy_s + k*kv_copy_s,
+ *                              compute  = (L-k)*restore_s     + k*kv_place_s
+ * over k = 0..L layers loaded as K/V (ties: the smaller k).  Host-only; all
+ * costs in seconds per layer, finite and >= 0.
+ *
+ * hcr_profile_layer_costs measures the four costs on the current GPU for
+ * n_tokens tokens, restoring groups of layers_per_chunk layers as the
+ * streamed restore does, with CUDA events on `stream` (mean of `reps` runs
+ * after `reps` warm-up runs).  It allocates device and pinned host buffers
+ * for one group (freed before it returns) and synchronises `stream`.
+ */
+typedef struct {
+  double restore_s;       /* GPU time to restore one layer from hidden states  */
+  double hidden_copy_s;   /* host-to-device time for one layer's hidden states */
+  double kv_copy_s;       /* host-to-device time for one layer's K and V       */
+  double kv_place_s;      /* GPU time to place one layer's K and V             */
+} hcr_layer_costs;
+
+typedef struct {
+  int32_t hidden_layers;  /* restored from hidden states (the first group) */
+  int32_t kv_layers;      /* loaded as saved K and V (the last group)     */
+  double transfer_s, compute_s, predicted_s;   /* predicted = max of the two */
+} hcr_layer_split;
+
+hcr_status hcr_plan_layer_split(const hcr_layer_costs* costs, int32_t n_layers,
+                                hcr_layer_split* out);
+hcr_status hcr_profile_layer_costs(hcr_handle* h, int32_t n_tokens, int32_t layers_per_chunk,
+                                   int32_t reps, void* stream, hcr_layer_costs* out);
+
+/*
+ * hcr_restore_streamed_split -- the layer-split restore from host memory.
+ * Layers [layer_begin, split_layer) are restored from hidden states
+ *     hidden_host: HOST (pinned) [split_layer - layer_begin][n_tokens][d_model]
+ * and layers [split_layer, layer_end) are placed from saved K/V
+ *     kv_host:     HOST (pinned) [layer_end - split_layer][2][n_tokens][d_kv]
+ * (the hcr_load_kv layout).  Both go through the staging ring of
+ * hcr_restore_streamed on the handle's copy stream: one slot holds a group of
+ * layers_per_chunk hidden-state layers, or as many K/V layers as fit (at
+ * least one; the slot size is the larger of the two).  The K/V groups are
+ * spread evenly among the hidden-state groups so that transfer and compute
+ * overlap throughout.  The caches are bit-identical to hcr_restore over the
+ * hidden-state layers and to hcr_load_kv over the K/V layers.  The workspace
+ * needs hcr_workspace_bytes(h, n_tokens, min(layers_per_chunk, hidden
+ * layers)) bytes (at least one layer's).  Other arguments are as in
+ * hcr_restore_streamed; split_layer = layer_end is a plain streamed restore.
+ */
+hcr_status hcr_restore_streamed_split(hcr_handle* h, const void* hidden_host,
+                                      const void* kv_host, int32_t layer_begin,
+                                      int32_t split_layer, int32_t layer_end, int32_t n_req,
+                                      int32_t n_tokens, const int32_t* cu_seqlens,
+                                      const int32_t* start_pos, const int32_t* block_table,
+                                      int32_t max_blocks_per_req, void* k_cache, void* v_cache,
+                                      const hcr_cache_layout* layout, void* staging,
+                                      size_t staging_bytes, int32_t layers_per_chunk,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * hcr_restore_no_alloc -- hcr_restore without a caller-provided workspace.
  *
  * The paper has no counterpart to this call; it exists for callers of this

@@ -54,6 +54,17 @@ class hcr_chunk_source(ctypes.Structure):
                 ("start_pos", ctypes.c_void_p)]
 
 
+class hcr_layer_costs(ctypes.Structure):
+    _fields_ = [("restore_s", ctypes.c_double), ("hidden_copy_s", ctypes.c_double),
+                ("kv_copy_s", ctypes.c_double), ("kv_place_s", ctypes.c_double)]
+
+
+class hcr_layer_split(ctypes.Structure):
+    _fields_ = [("hidden_layers", ctypes.c_int32), ("kv_layers", ctypes.c_int32),
+                ("transfer_s", ctypes.c_double), ("compute_s", ctypes.c_double),
+                ("predicted_s", ctypes.c_double)]
+
+
 class HcrError(RuntimeError):
     def __init__(self, status: int, where: str, message: str):
         super().__init__(f"{where}: {message}")
@@ -94,6 +105,19 @@ lib.hcr_save_hidden.restype = ctypes.c_int
 lib.hcr_restore_streamed_chunks.argtypes = [_vp, ctypes.POINTER(hcr_chunk_source)] + \
     _RESTORE_ARGTYPES[2:13] + [_vp, ctypes.c_size_t, _i32, _vp, ctypes.c_size_t, _vp]
 lib.hcr_restore_streamed_chunks.restype = ctypes.c_int
+for _name in ("hcr_load_kv", "hcr_save_kv"):
+    getattr(lib, _name).argtypes = _RESTORE_ARGTYPES
+    getattr(lib, _name).restype = ctypes.c_int
+lib.hcr_plan_layer_split.argtypes = [ctypes.POINTER(hcr_layer_costs), _i32,
+                                     ctypes.POINTER(hcr_layer_split)]
+lib.hcr_plan_layer_split.restype = ctypes.c_int
+lib.hcr_profile_layer_costs.argtypes = [_vp, _i32, _i32, _i32, _vp,
+                                        ctypes.POINTER(hcr_layer_costs)]
+lib.hcr_profile_layer_costs.restype = ctypes.c_int
+lib.hcr_restore_streamed_split.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp,
+                                           _vp, _i32, _vp, _vp, ctypes.POINTER(hcr_cache_layout),
+                                           _vp, ctypes.c_size_t, _i32, _vp, ctypes.c_size_t, _vp]
+lib.hcr_restore_streamed_split.restype = ctypes.c_int
 lib.hcr_restore_no_alloc.argtypes = _RESTORE_ARGTYPES[:13] + [_vp]
 lib.hcr_restore_no_alloc.restype = ctypes.c_int
 HCR_NO_ALLOC_SCRATCH_BYTES = 16 << 20
@@ -239,6 +263,61 @@ def hcr_restore_streamed_chunks(handle, source: hcr_chunk_source, layer_begin, l
         layers_per_chunk, _ptr(workspace), workspace_bytes, _stream_ptr(stream))
     if check:
         _check(st, "hcr_restore_streamed_chunks")
+    return st
+
+
+def hcr_load_kv(handle, kv, layer_begin, layer_end, n_req, n_tokens, cu_seqlens, start_pos,
+                block_table, max_blocks_per_req, k_cache, v_cache, layout, workspace,
+                workspace_bytes, stream=None, *, check: bool = True) -> int:
+    """Places saved K/V rows ([layers][2][tokens][d_kv]) into the paged cache."""
+    return _restore_call(lib.hcr_load_kv, "hcr_load_kv", handle, kv, layer_begin, layer_end,
+                         n_req, n_tokens, cu_seqlens, start_pos, block_table,
+                         max_blocks_per_req, k_cache, v_cache, layout, workspace,
+                         workspace_bytes, stream, check)
+
+
+def hcr_save_kv(handle, kv, layer_begin, layer_end, n_req, n_tokens, cu_seqlens, start_pos,
+                block_table, max_blocks_per_req, k_cache, v_cache, layout, workspace,
+                workspace_bytes, stream=None, *, check: bool = True) -> int:
+    """Copies the requests' K/V rows out of the paged cache ([layers][2][tokens][d_kv])."""
+    return _restore_call(lib.hcr_save_kv, "hcr_save_kv", handle, kv, layer_begin, layer_end,
+                         n_req, n_tokens, cu_seqlens, start_pos, block_table,
+                         max_blocks_per_req, k_cache, v_cache, layout, workspace,
+                         workspace_bytes, stream, check)
+
+
+def hcr_plan_layer_split(costs: hcr_layer_costs, n_layers: int) -> hcr_layer_split:
+    """Min-max layer split between hidden-state restore and K/V load (host only)."""
+    out = hcr_layer_split()
+    _check(lib.hcr_plan_layer_split(ctypes.byref(costs), n_layers, ctypes.byref(out)),
+           "hcr_plan_layer_split")
+    return out
+
+
+def hcr_profile_layer_costs(handle, n_tokens: int, layers_per_chunk: int, reps: int,
+                            stream=None) -> hcr_layer_costs:
+    """Per-layer costs measured on the current GPU for n_tokens tokens."""
+    out = hcr_layer_costs()
+    _check(lib.hcr_profile_layer_costs(handle, n_tokens, layers_per_chunk, reps,
+                                       _stream_ptr(stream), ctypes.byref(out)),
+           "hcr_profile_layer_costs")
+    return out
+
+
+def hcr_restore_streamed_split(handle, hidden_host, kv_host, layer_begin, split_layer, layer_end,
+                               n_req, n_tokens, cu_seqlens, start_pos, block_table,
+                               max_blocks_per_req, k_cache, v_cache, layout, staging,
+                               staging_bytes, layers_per_chunk, workspace, workspace_bytes,
+                               stream=None, *, check: bool = True) -> int:
+    """Layer-split streamed restore: hidden states below split_layer, saved K/V above."""
+    st = lib.hcr_restore_streamed_split(
+        handle, _ptr(hidden_host), _ptr(kv_host), layer_begin, split_layer, layer_end, n_req,
+        n_tokens, _ptr(cu_seqlens), _ptr(start_pos), _ptr(block_table), max_blocks_per_req,
+        _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout) if layout is not None else None,
+        _ptr(staging), staging_bytes, layers_per_chunk, _ptr(workspace), workspace_bytes,
+        _stream_ptr(stream))
+    if check:
+        _check(st, "hcr_restore_streamed_split")
     return st
 
 

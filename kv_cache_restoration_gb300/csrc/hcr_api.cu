@@ -121,8 +121,11 @@ struct RestoreArgs {
   cudaStream_t stream;
 };
 
-// Returns HCR_OK with *empty set when there is nothing to do.
-hcr_status validate_restore(const hcr_handle* h, const RestoreArgs& a, bool* empty) {
+// Returns HCR_OK with *empty set when there is nothing to do.  `stats` says
+// whether the workspace must hold norm statistics for the layer range, not
+// only the slot map.
+hcr_status validate_restore(const hcr_handle* h, const RestoreArgs& a, bool* empty,
+                            bool stats = true) {
   *empty = false;
   if (!h) return fail(HCR_ERR_INVALID_ARG, "handle is NULL");
   const hcr_model_dims& d = h->impl.dims;
@@ -154,8 +157,8 @@ hcr_status validate_restore(const hcr_handle* h, const RestoreArgs& a, bool* emp
                 (long long)a.layout->layer_stride_elems, (long long)dense);
   if (a.layout->layer_stride_elems % 8)
     return fail(HCR_ERR_INVALID_ARG, "layer_stride_elems must be a multiple of 8");
-  const size_t need =
-      workspace_layout(a.n_tokens, a.layer_end - a.layer_begin, d.norm == HCR_NORM_LAYER).total;
+  const size_t need = workspace_layout(a.n_tokens, stats ? a.layer_end - a.layer_begin : 0,
+                                       d.norm == HCR_NORM_LAYER).total;
   if (!a.workspace) return fail(HCR_ERR_WORKSPACE, "workspace is NULL");
   if (!aligned(a.workspace, 256))
     return fail(HCR_ERR_WORKSPACE, "workspace must be 256-byte aligned");
@@ -164,10 +167,11 @@ hcr_status validate_restore(const hcr_handle* h, const RestoreArgs& a, bool* emp
   return HCR_OK;
 }
 
-hcr_status do_prepare(hcr_handle* h, const RestoreArgs& a) {
+// stats = false: the slot map only (the K/V row copies need no statistics).
+hcr_status do_prepare(hcr_handle* h, const RestoreArgs& a, bool stats = true) {
   const Handle& H = h->impl;
   const hcr_model_dims& d = H.dims;
-  const int32_t nl = a.layer_end - a.layer_begin;
+  const int32_t nl = stats ? a.layer_end - a.layer_begin : 0;
   const WorkspaceLayout w = workspace_layout(a.n_tokens, nl, d.norm == HCR_NORM_LAYER);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   PrepareParams p{};
@@ -477,6 +481,60 @@ hcr_status hcr_restore(hcr_handle* h, const void* hidden, int32_t layer_begin, i
   st = do_prepare(h, a);
   if (st != HCR_OK) return st;
   return do_project(h, a);
+}
+
+static hcr_status kv_rows(hcr_handle* h, const RestoreArgs& a, bool to_cache, const char* what) {
+  bool empty = false;
+  hcr_status st = validate_restore(h, a, &empty, /*stats=*/false);
+  if (st != HCR_OK || empty) return st;
+  void* dense = nullptr;
+  st = device_view(h->impl, const_cast<void*>(a.hidden), what, &dense);
+  if (st != HCR_OK) return st;
+  st = do_prepare(h, a, /*stats=*/false);
+  if (st != HCR_OK) return st;
+  const hcr_model_dims& d = h->impl.dims;
+  const int64_t row = int64_t(d.n_kv_heads) * d.head_dim;
+  const int64_t stride = a.layout->layer_stride_elems
+                             ? a.layout->layer_stride_elems
+                             : int64_t(a.layout->num_blocks) * a.layout->block_size * row;
+  const WorkspaceLayout w = workspace_layout(a.n_tokens, 0, false);
+  KvRowsParams p{};
+  p.slot = reinterpret_cast<const int64_t*>(static_cast<uint8_t*>(a.workspace) + w.slot_off);
+  p.dense = static_cast<uint4*>(dense);
+  p.k_cache = a.k_cache;
+  p.v_cache = a.v_cache;
+  p.layer_stride_vecs = stride / 8;
+  p.row_vecs = int32_t(row / 8);
+  p.n_tokens = a.n_tokens;
+  p.n_layers = a.layer_end - a.layer_begin;
+  cudaError_t e = launch_kv_rows(p, to_cache, h->impl.num_sms, a.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "K/V row copy launch");
+  return HCR_OK;
+}
+
+hcr_status hcr_load_kv(hcr_handle* h, const void* kv, int32_t layer_begin, int32_t layer_end,
+                       int32_t n_req, int32_t n_tokens, const int32_t* cu_seqlens,
+                       const int32_t* start_pos, const int32_t* block_table,
+                       int32_t max_blocks_per_req, void* k_cache, void* v_cache,
+                       const hcr_cache_layout* layout, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  RestoreArgs a{kv,         layer_begin, layer_end,   n_req,   n_tokens,  cu_seqlens,
+                start_pos,  block_table, max_blocks_per_req, k_cache, v_cache,   layout,
+                workspace,  workspace_bytes, static_cast<cudaStream_t>(stream)};
+  return kv_rows(h, a, /*to_cache=*/true, "kv");
+}
+
+hcr_status hcr_save_kv(hcr_handle* h, void* kv, int32_t layer_begin, int32_t layer_end,
+                       int32_t n_req, int32_t n_tokens, const int32_t* cu_seqlens,
+                       const int32_t* start_pos, const int32_t* block_table,
+                       int32_t max_blocks_per_req, const void* k_cache, const void* v_cache,
+                       const hcr_cache_layout* layout, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  RestoreArgs a{kv,         layer_begin, layer_end,   n_req,   n_tokens,  cu_seqlens,
+                start_pos,  block_table, max_blocks_per_req, const_cast<void*>(k_cache),
+                const_cast<void*>(v_cache), layout, workspace, workspace_bytes,
+                static_cast<cudaStream_t>(stream)};
+  return kv_rows(h, a, /*to_cache=*/false, "kv");
 }
 
 hcr_status hcr_check_device_error(hcr_handle* h, void* stream, uint32_t* flags) {

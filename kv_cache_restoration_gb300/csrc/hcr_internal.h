@@ -146,6 +146,18 @@ struct ProjectParams {
   uint32_t debug_stall;
 };
 
+// Rows of K and V between the paged cache and a dense [layer][K|V][token][row]
+// store (hcr_kv.cu).  Pointers to host memory are the device's mapped view.
+struct KvRowsParams {
+  const int64_t* slot;     // [T] from the prepare kernel; -1 rows are skipped
+  uint4* dense;            // [n_layers][2][T][row_vecs]
+  void* k_cache;           // base of the first layer
+  void* v_cache;
+  int64_t layer_stride_vecs;
+  int32_t row_vecs;        // n_kv_heads * head_dim / 8
+  int32_t n_tokens, n_layers;
+};
+
 // Records a message for hcr_last_error() on this host thread; returns s.
 hcr_status set_last_error(hcr_status s, const char* fmt, ...);
 
@@ -153,6 +165,11 @@ hcr_status set_last_error(hcr_status s, const char* fmt, ...);
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t s);
 cudaError_t launch_project(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
                            const ProjectParams& p, int grid, bool pair, cudaStream_t s);
+cudaError_t launch_kv_rows(const KvRowsParams& p, bool to_cache, int num_sms, cudaStream_t s);
+// The device address of caller memory that may live on the host (mapped pinned
+// memory, or pageable memory when the device can reach it); an error status
+// names `what` when the device cannot address it.
+hcr_status device_view(const Handle& H, void* ptr, const char* what, void** out);
 // Co-resident clusters of the CTA-pair variant on the current device (< 0 on error).
 int project_pair_clusters(int dtype);
 cudaError_t launch_pack_weights(const void* w_k, const void* w_v, const void* gamma, void* dst,

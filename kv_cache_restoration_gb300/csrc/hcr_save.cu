@@ -96,6 +96,33 @@ __global__ void __launch_bounds__(kSaveThreads) save_kernel(const SaveParams p) 
 }
 
 }  // namespace
+
+// Host memory is used through its device address; memory the device cannot
+// reach (unregistered pageable memory without pageable-memory access) is
+// refused instead of letting a kernel fault on it.
+hcr_status device_view(const Handle& H, void* ptr, const char* what, void** out) {
+  *out = ptr;
+  cudaPointerAttributes attr{};
+  cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return set_last_error(HCR_ERR_CUDA, "cudaPointerGetAttributes(%s): %s", what,
+                          cudaGetErrorString(e));
+  }
+  if (attr.type == cudaMemoryTypeHost) {
+    if (!attr.devicePointer)
+      return set_last_error(HCR_ERR_INVALID_ARG, "%s host memory is not mapped", what);
+    *out = attr.devicePointer;
+  } else if (attr.type == cudaMemoryTypeUnregistered) {
+    int pageable = 0;
+    cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, H.device);
+    if (!pageable)
+      return set_last_error(HCR_ERR_INVALID_ARG,
+                            "%s is unregistered host memory the device cannot access", what);
+  }
+  return HCR_OK;
+}
+
 }  // namespace hcr
 
 using namespace hcr;
@@ -125,30 +152,9 @@ extern "C" hcr_status hcr_save_hidden(hcr_handle* h, const void* hidden, int32_t
   if (max_chunks_per_req < 1 || chunk_tokens < 1 || num_chunks < 1)
     return set_last_error(HCR_ERR_INVALID_ARG,
                           "max_chunks_per_req, chunk_tokens and num_chunks must be >= 1");
-  // The store may be host memory: use its device address, and refuse memory
-  // the device cannot reach (unregistered pageable memory without
-  // pageable-memory access) instead of letting the kernel fault on it.
-  void* store = chunk_store;
-  {
-    cudaPointerAttributes attr{};
-    cudaError_t e = cudaPointerGetAttributes(&attr, chunk_store);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return set_last_error(HCR_ERR_CUDA, "cudaPointerGetAttributes(chunk_store): %s",
-                            cudaGetErrorString(e));
-    }
-    if (attr.type == cudaMemoryTypeHost) {
-      if (!attr.devicePointer)
-        return set_last_error(HCR_ERR_INVALID_ARG, "chunk_store host memory is not mapped");
-      store = attr.devicePointer;
-    } else if (attr.type == cudaMemoryTypeUnregistered) {
-      int pageable = 0;
-      cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, h->impl.device);
-      if (!pageable)
-        return set_last_error(HCR_ERR_INVALID_ARG,
-                              "chunk_store is unregistered host memory the device cannot access");
-    }
-  }
+  void* store = nullptr;
+  hcr_status st = device_view(h->impl, chunk_store, "chunk_store", &store);
+  if (st != HCR_OK) return st;
   SaveParams p{};
   p.hidden = static_cast<const uint16_t*>(hidden);
   p.cu_seqlens = cu_seqlens;

@@ -75,34 +75,35 @@ hcr_status ensure_resources(Handle& H, StreamedRes** out) {
   return HCR_OK;
 }
 
-// Copies the hidden states of layers [l0, l0 + nl) (relative to the restore's
-// first layer) into `dst` laid out [nl][n_tokens][d_model], on `copy`.
-using CopyFn = std::function<cudaError_t(void* dst, int32_t l0, int32_t nl, cudaStream_t copy)>;
+// One unit of the pipeline: layers [l0, l0 + nl) (relative to the call's
+// first layer), restored from hidden states or, for kv, placed from saved K/V.
+struct Item {
+  bool kv;
+  int32_t l0, nl;
+};
 
-hcr_status streamed_pipeline(hcr_handle* h, int32_t layer_begin, int32_t layer_end,
-                             int32_t n_req, int32_t n_tokens, const int32_t* cu_seqlens,
-                             const int32_t* start_pos, const int32_t* block_table,
-                             int32_t max_blocks_per_req, void* k_cache, void* v_cache,
-                             const hcr_cache_layout* layout, void* staging, size_t staging_bytes,
-                             int32_t layers_per_chunk, void* workspace, size_t workspace_bytes,
-                             void* stream, const CopyFn& copy_layers) {
+// Copies an item's host data into `dst` on `copy`: hidden states laid out
+// [nl][n_tokens][d_model], or K/V laid out [nl][2][n_tokens][d_kv].
+using CopyFn = std::function<cudaError_t(const Item& it, void* dst, cudaStream_t copy)>;
+
+hcr_status run_pipeline(hcr_handle* h, const std::vector<Item>& items, size_t slot_bytes,
+                        int32_t layer_begin, int32_t n_req, int32_t n_tokens,
+                        const int32_t* cu_seqlens, const int32_t* start_pos,
+                        const int32_t* block_table, int32_t max_blocks_per_req, void* k_cache,
+                        void* v_cache, const hcr_cache_layout* layout, void* staging,
+                        size_t staging_bytes, size_t workspace_need, void* workspace,
+                        size_t workspace_bytes, void* stream, const CopyFn& copy_item) {
   const hcr_model_dims& d = h->impl.dims;
   if (!layout) return set_last_error(HCR_ERR_INVALID_ARG, "layout is NULL");
-  if (layers_per_chunk < 1)
-    return set_last_error(HCR_ERR_INVALID_ARG, "layers_per_chunk must be >= 1");
-  const int32_t n_layers = layer_end - layer_begin;
-  const int32_t chunk = std::min(layers_per_chunk, n_layers);
-  const size_t layer_bytes = size_t(n_tokens) * size_t(d.d_model) * 2;
-  const size_t chunk_bytes = layer_bytes * size_t(chunk);
   if (!staging || reinterpret_cast<uintptr_t>(staging) % 256)
     return set_last_error(HCR_ERR_WORKSPACE, "staging must be non-NULL and 256-byte aligned");
-  const int slots = int(std::min<size_t>(staging_bytes / chunk_bytes, kMaxStagingSlots));
+  const int slots = int(std::min<size_t>(staging_bytes / slot_bytes, kMaxStagingSlots));
   if (slots < 1)
-    return set_last_error(HCR_ERR_WORKSPACE, "staging has %zu bytes; one chunk of %d layers "
-                          "needs %zu", staging_bytes, chunk, chunk_bytes);
-  if (workspace_bytes < hcr_workspace_bytes(h, n_tokens, chunk))
+    return set_last_error(HCR_ERR_WORKSPACE, "staging has %zu bytes; one slot needs %zu",
+                          staging_bytes, slot_bytes);
+  if (workspace_bytes < workspace_need)
     return set_last_error(HCR_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu for a chunk",
-                          workspace_bytes, hcr_workspace_bytes(h, n_tokens, chunk));
+                          workspace_bytes, workspace_need);
   const int64_t row = int64_t(d.n_kv_heads) * d.head_dim;
   const int64_t stride = layout->layer_stride_elems
                              ? layout->layer_stride_elems
@@ -124,29 +125,54 @@ hcr_status streamed_pipeline(hcr_handle* h, int32_t layer_begin, int32_t layer_e
   if ((e = cudaStreamWaitEvent(r->copy, r->start, 0)) != cudaSuccess)
     return cuda_err(e, "stream wait");
   uint8_t* ring = static_cast<uint8_t*>(staging);
-  int c = 0;
-  for (int32_t l0 = 0; l0 < n_layers; l0 += chunk, ++c) {
-    const int32_t nl = std::min(chunk, n_layers - l0);
-    const int slot = c % slots;
-    void* dst = ring + size_t(slot) * chunk_bytes;
-    if (c >= slots && (e = cudaStreamWaitEvent(r->copy, r->done[slot], 0)) != cudaSuccess)
+  for (size_t c = 0; c < items.size(); ++c) {
+    const Item& it = items[c];
+    const int slot = int(c % size_t(slots));
+    void* dst = ring + size_t(slot) * slot_bytes;
+    if (c >= size_t(slots) &&
+        (e = cudaStreamWaitEvent(r->copy, r->done[slot], 0)) != cudaSuccess)
       return cuda_err(e, "stream wait");
-    if ((e = copy_layers(dst, l0, nl, r->copy)) != cudaSuccess)
-      return cuda_err(e, "hidden-state copy");
+    if ((e = copy_item(it, dst, r->copy)) != cudaSuccess) return cuda_err(e, "host copy");
     if ((e = cudaEventRecord(r->copied[slot], r->copy)) != cudaSuccess)
       return cuda_err(e, "event record");
     if ((e = cudaStreamWaitEvent(s, r->copied[slot], 0)) != cudaSuccess)
       return cuda_err(e, "stream wait");
-    st = hcr_restore(h, dst, layer_begin + l0, layer_begin + l0 + nl, n_req, n_tokens,
-                     cu_seqlens, start_pos, block_table, max_blocks_per_req,
-                     static_cast<uint16_t*>(k_cache) + int64_t(l0) * stride,
-                     static_cast<uint16_t*>(v_cache) + int64_t(l0) * stride, layout, workspace,
-                     workspace_bytes, stream);
+    auto* kc = static_cast<uint16_t*>(k_cache) + int64_t(it.l0) * stride;
+    auto* vc = static_cast<uint16_t*>(v_cache) + int64_t(it.l0) * stride;
+    const int32_t lb = layer_begin + it.l0;
+    st = it.kv ? hcr_load_kv(h, dst, lb, lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos,
+                             block_table, max_blocks_per_req, kc, vc, layout, workspace,
+                             workspace_bytes, stream)
+               : hcr_restore(h, dst, lb, lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos,
+                             block_table, max_blocks_per_req, kc, vc, layout, workspace,
+                             workspace_bytes, stream);
     if (st != HCR_OK) return st;
     if ((e = cudaEventRecord(r->done[slot], s)) != cudaSuccess)
       return cuda_err(e, "event record");
   }
   return HCR_OK;
+}
+
+// Hidden-state groups of `layers_per_chunk` layers over [layer_begin, layer_end).
+hcr_status hidden_pipeline(hcr_handle* h, int32_t layer_begin, int32_t layer_end, int32_t n_req,
+                           int32_t n_tokens, const int32_t* cu_seqlens, const int32_t* start_pos,
+                           const int32_t* block_table, int32_t max_blocks_per_req,
+                           void* k_cache, void* v_cache, const hcr_cache_layout* layout,
+                           void* staging, size_t staging_bytes, int32_t layers_per_chunk,
+                           void* workspace, size_t workspace_bytes, void* stream,
+                           const CopyFn& copy_item) {
+  if (layers_per_chunk < 1)
+    return set_last_error(HCR_ERR_INVALID_ARG, "layers_per_chunk must be >= 1");
+  const int32_t n_layers = layer_end - layer_begin;
+  const int32_t chunk = std::min(layers_per_chunk, n_layers);
+  std::vector<Item> items;
+  for (int32_t l0 = 0; l0 < n_layers; l0 += chunk)
+    items.push_back({false, l0, std::min(chunk, n_layers - l0)});
+  const size_t slot_bytes = size_t(chunk) * size_t(n_tokens) * size_t(h->impl.dims.d_model) * 2;
+  return run_pipeline(h, items, slot_bytes, layer_begin, n_req, n_tokens, cu_seqlens, start_pos,
+                      block_table, max_blocks_per_req, k_cache, v_cache, layout, staging,
+                      staging_bytes, hcr_workspace_bytes(h, n_tokens, chunk), workspace,
+                      workspace_bytes, stream, copy_item);
 }
 
 }  // namespace
@@ -170,13 +196,12 @@ extern "C" hcr_status hcr_restore_streamed(
   if (!hidden_host) return set_last_error(HCR_ERR_INVALID_ARG, "hidden_host is NULL");
   const uint8_t* src = static_cast<const uint8_t*>(hidden_host);
   const size_t layer_bytes = size_t(n_tokens) * size_t(d.d_model) * 2;
-  return streamed_pipeline(
+  return hidden_pipeline(
       h, layer_begin, layer_end, n_req, n_tokens, cu_seqlens, start_pos, block_table,
       max_blocks_per_req, k_cache, v_cache, layout, staging, staging_bytes, layers_per_chunk,
-      workspace, workspace_bytes, stream,
-      [&](void* dst, int32_t l0, int32_t nl, cudaStream_t copy) {
-        return cudaMemcpyAsync(dst, src + size_t(l0) * layer_bytes, size_t(nl) * layer_bytes,
-                               cudaMemcpyHostToDevice, copy);
+      workspace, workspace_bytes, stream, [&](const Item& it, void* dst, cudaStream_t copy) {
+        return cudaMemcpyAsync(dst, src + size_t(it.l0) * layer_bytes,
+                               size_t(it.nl) * layer_bytes, cudaMemcpyHostToDevice, copy);
       });
 }
 
@@ -254,11 +279,11 @@ extern "C" hcr_status hcr_restore_streamed_chunks(
   const uint8_t* store = static_cast<const uint8_t*>(src.store);
   const size_t layer_in_chunk = size_t(C) * row_bytes;       // next layer inside a chunk
   const size_t layer_in_slot = size_t(n_tokens) * row_bytes;  // next layer in the slot
-  return streamed_pipeline(
+  return hidden_pipeline(
       h, layer_begin, layer_end, n_req, n_tokens, cu_seqlens, start_pos, block_table,
       max_blocks_per_req, k_cache, v_cache, layout, staging, staging_bytes, layers_per_chunk,
-      workspace, workspace_bytes, stream,
-      [&](void* dst, int32_t l0, int32_t nl, cudaStream_t copy) {
+      workspace, workspace_bytes, stream, [&](const Item& it, void* dst, cudaStream_t copy) {
+        const int32_t l0 = it.l0, nl = it.nl;
         uint8_t* slot = static_cast<uint8_t*>(dst);
         cudaError_t e = cudaSuccess;
         for (const Run& run : runs) {
@@ -279,5 +304,62 @@ extern "C" hcr_status hcr_restore_streamed_chunks(
           if (e != cudaSuccess) return e;
         }
         return cudaSuccess;
+      });
+}
+
+extern "C" hcr_status hcr_restore_streamed_split(
+    hcr_handle* h, const void* hidden_host, const void* kv_host, int32_t layer_begin,
+    int32_t split_layer, int32_t layer_end, int32_t n_req, int32_t n_tokens,
+    const int32_t* cu_seqlens, const int32_t* start_pos, const int32_t* block_table,
+    int32_t max_blocks_per_req, void* k_cache, void* v_cache, const hcr_cache_layout* layout,
+    void* staging, size_t staging_bytes, int32_t layers_per_chunk, void* workspace,
+    size_t workspace_bytes, void* stream) {
+  if (!h) return set_last_error(HCR_ERR_INVALID_ARG, "handle is NULL");
+  const hcr_model_dims& d = h->impl.dims;
+  if (layer_begin < 0 || split_layer < layer_begin || layer_end < split_layer ||
+      layer_end > d.n_layers)
+    return set_last_error(HCR_ERR_INVALID_ARG,
+                          "need 0 <= layer_begin <= split_layer <= layer_end <= %d, got %d, %d, %d",
+                          d.n_layers, layer_begin, split_layer, layer_end);
+  if (n_tokens < 0) return set_last_error(HCR_ERR_INVALID_ARG, "n_tokens must be >= 0");
+  if (n_tokens == 0 || layer_end == layer_begin) return HCR_OK;
+  if (layers_per_chunk < 1)
+    return set_last_error(HCR_ERR_INVALID_ARG, "layers_per_chunk must be >= 1");
+  const int32_t n_hid = split_layer - layer_begin, n_kv = layer_end - split_layer;
+  if ((n_hid > 0 && !hidden_host) || (n_kv > 0 && !kv_host))
+    return set_last_error(HCR_ERR_INVALID_ARG, "hidden_host/kv_host is NULL");
+  const size_t hid_layer = size_t(n_tokens) * size_t(d.d_model) * 2;
+  const size_t kv_layer = size_t(n_tokens) * 2 * size_t(d.n_kv_heads) * d.head_dim * 2;
+  // A slot holds one hidden-state group, or as many whole K/V layers as fit
+  // (at least one).
+  const int32_t ch = std::min(layers_per_chunk, n_hid);
+  const size_t slot_bytes = std::max(size_t(ch) * hid_layer, n_kv > 0 ? kv_layer : size_t(0));
+  const int32_t ck = n_kv > 0 ? int32_t(std::min<size_t>(size_t(n_kv), slot_bytes / kv_layer)) : 0;
+  std::vector<Item> hid_items, kv_items, items;
+  for (int32_t l0 = 0; l0 < n_hid; l0 += ch) hid_items.push_back({false, l0, std::min(ch, n_hid - l0)});
+  for (int32_t l0 = 0; l0 < n_kv; l0 += ck)
+    kv_items.push_back({true, n_hid + l0, std::min(ck, n_kv - l0)});
+  // Spread the K/V groups evenly among the hidden-state groups so both the
+  // copy stream and the compute stream stay busy: item i of a list of n sits
+  // at (i + 1/2) / n, and the hidden-state group goes first on a tie.
+  const size_t a = hid_items.size(), b = kv_items.size();
+  for (size_t i = 0, j = 0; i < a || j < b;) {
+    if (j == b || (i < a && (2 * i + 1) * b <= (2 * j + 1) * a))
+      items.push_back(hid_items[i++]);
+    else
+      items.push_back(kv_items[j++]);
+  }
+  const uint8_t* hid = static_cast<const uint8_t*>(hidden_host);
+  const uint8_t* kv = static_cast<const uint8_t*>(kv_host);
+  return run_pipeline(
+      h, items, slot_bytes, layer_begin, n_req, n_tokens, cu_seqlens, start_pos, block_table,
+      max_blocks_per_req, k_cache, v_cache, layout, staging, staging_bytes,
+      hcr_workspace_bytes(h, n_tokens, std::max(ch, 1)), workspace, workspace_bytes, stream,
+      [&](const Item& it, void* dst, cudaStream_t copy) {
+        if (it.kv)
+          return cudaMemcpyAsync(dst, kv + size_t(it.l0 - n_hid) * kv_layer,
+                                 size_t(it.nl) * kv_layer, cudaMemcpyHostToDevice, copy);
+        return cudaMemcpyAsync(dst, hid + size_t(it.l0) * hid_layer, size_t(it.nl) * hid_layer,
+                               cudaMemcpyHostToDevice, copy);
       });
 }

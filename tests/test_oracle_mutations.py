@@ -214,3 +214,70 @@ def test_planted_save_mistake_is_caught(monkeypatch, attr, mutant):
         except (AssertionError, ValueError, IndexError):
             failed += 1
     assert failed, f"no pin caught {mutant.__name__}"
+
+
+# ----------------------------------------------------------------------------- layer split
+from oracle import split as SP  # noqa: E402
+from tests import test_oracle_split as TSP  # noqa: E402
+
+SPLIT_ORIG = {"pipeline_totals": SP.pipeline_totals, "plan_layer_split": SP.plan_layer_split,
+              "kv_rows_from_cache": SP.kv_rows_from_cache}
+
+
+def _totals_copies_swapped(c, n_layers, kv_layers):
+    return SPLIT_ORIG["pipeline_totals"](
+        SP.LayerCosts(c.restore, c.kv_copy, c.hidden_copy, c.kv_place), n_layers, kv_layers)
+
+
+def _totals_place_as_restore(c, n_layers, kv_layers):
+    return SPLIT_ORIG["pipeline_totals"](
+        SP.LayerCosts(c.restore, c.hidden_copy, c.kv_copy, c.restore), n_layers, kv_layers)
+
+
+def _plan_min_of_totals(c, n_layers):
+    best = None
+    for k in range(n_layers + 1):
+        tr, co = SP.pipeline_totals(c, n_layers, k)
+        t = min(tr, co)
+        if best is None or t < best.predicted:
+            best = SP.Split(n_layers - k, k, tr, co, t)
+    return best
+
+
+def _plan_never_all_kv(c, n_layers):
+    best = None
+    for k in range(max(n_layers, 1)):
+        tr, co = SP.pipeline_totals(c, n_layers, k)
+        t = max(tr, co)
+        if best is None or t < best.predicted:
+            best = SP.Split(n_layers - k, k, tr, co, t)
+    return best
+
+
+def _rows_k_v_swapped(k_cache, v_cache, *a):
+    return SPLIT_ORIG["kv_rows_from_cache"](v_cache, k_cache, *a)
+
+
+SPLIT_PINS = [TSP.test_hand_worked_split, lambda: TSP.test_crossing_point_closed_form(3),
+              TSP.test_transfer_bound_keeps_every_layer_on_hidden_states,
+              TSP.test_cheaper_kv_everywhere_loads_every_layer,
+              TSP.test_ties_keep_fewer_kv_layers_and_empty_model,
+              TSP.test_kv_rows_round_trip_and_untouched_slots]
+
+
+@pytest.mark.parametrize("attr,mutant", [("pipeline_totals", _totals_copies_swapped),
+                                         ("pipeline_totals", _totals_place_as_restore),
+                                         ("plan_layer_split", _plan_min_of_totals),
+                                         ("plan_layer_split", _plan_never_all_kv),
+                                         ("kv_rows_from_cache", _rows_k_v_swapped)],
+                         ids=["copies_swapped", "place_as_restore", "min_of_totals",
+                              "never_all_kv", "rows_k_v_swapped"])
+def test_planted_split_mistake_is_caught(monkeypatch, attr, mutant):
+    monkeypatch.setattr(SP, attr, mutant)
+    failed = 0
+    for pin in SPLIT_PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            failed += 1
+    assert failed, f"no pin caught {mutant.__name__}"

@@ -311,6 +311,37 @@ def gpu_arm(args, rank, world, local_rank):
                                  ctab_np.ctypes.data, int(ctab_np.shape[1]), cu_np.ctypes.data,
                                  start_np.ctypes.data)
         src._keep = (store, ctab_np, cu_np, start_np)
+    split_plan = None
+    if args.e2e_source == "split" and e2e_steps > 0:
+        # Bubble-free layer split: profile the per-layer costs on this GPU,
+        # plan, and keep the upper layers' K/V (as the restore left them in
+        # the cache) in pinned host memory; the lower layers stay hidden states.
+        costs = B.hcr_profile_layer_costs(r.handle, T, chunk, 5, stream)
+        split_plan = B.hcr_plan_layer_split(costs, L)
+        if args.split_layer >= 0:
+            n_kv = L - min(args.split_layer, L)
+        else:
+            n_kv = split_plan.kv_layers
+        split = L - n_kv
+        d_kv = s.n_kv_heads * s.head_dim
+        kv_host = torch.empty((max(n_kv, 1), 2, T, d_kv), dtype=case.hidden.dtype).pin_memory()
+        if n_kv:
+            B.hcr_save_kv(r.handle, kv_host, split, L, w.n_req, T, case.cu, case.start, case.table,
+                          lay.max_blocks, case.k_cache[split:], case.v_cache[split:], layout, ws,
+                          ws.numel(), stream)
+        torch.cuda.synchronize(device)
+        hid_host_split = hidden_host[:max(split, 1)]
+        slot_bytes = max(min(chunk, split) * T * s.d_model * 2 if split else 0,
+                         2 * T * d_kv * 2 if n_kv else 0)
+        staging = torch.empty(args.e2e_slots * slot_bytes, dtype=torch.uint8, device=device)
+        h2d = (split * T * s.d_model + n_kv * 2 * T * d_kv) * 2 + sum(
+            m.numel() * m.element_size() for m in meta_host)
+        split_plan = dict(kv_layers=n_kv, hidden_layers=split,
+                          planned_kv_layers=split_plan.kv_layers,
+                          predicted_ms=split_plan.predicted_s * 1e3,
+                          costs_ms_per_layer={f: getattr(costs, f) * 1e3 for f in
+                                              ("restore_s", "hidden_copy_s", "kv_copy_s",
+                                               "kv_place_s")})
     t0 = time.perf_counter()
     for i in range(2 + e2e_steps if e2e_steps > 0 else 0):
         if i == 2:
@@ -318,7 +349,13 @@ def gpu_arm(args, rank, world, local_rank):
             t0 = time.perf_counter()
         for hm, dm in zip(meta_host, meta_dev):
             dm.copy_(hm, non_blocking=True)
-        if src is None:
+        if split_plan is not None:
+            B.hcr_restore_streamed_split(r.handle, hid_host_split, kv_host, 0,
+                                         split_plan["hidden_layers"], L, w.n_req, T, case.cu,
+                                         case.start, case.table, lay.max_blocks, case.k_cache,
+                                         case.v_cache, layout, staging, staging.numel(), chunk,
+                                         ws, ws.numel(), stream)
+        elif src is None:
             B.hcr_restore_streamed(r.handle, hidden_host, 0, L, w.n_req, T, case.cu,
                                    case.start, case.table, lay.max_blocks, case.k_cache,
                                    case.v_cache, layout, staging, staging.numel(), chunk, ws,
@@ -346,7 +383,8 @@ def gpu_arm(args, rank, world, local_rank):
     t_step, proj_ms, prep_ms, e2e_s = reduce_max_over_ranks([t_step, proj_ms, prep_ms, e2e_s],
                                                             device)
     return dict(w=w, t_step=t_step, proj_ms=proj_ms, prep_ms=prep_ms, e2e_s=e2e_s, h2d=h2d,
-                clocks=clk.summary(), launches=2 * args.steps, h2d_gbs=h2d_gbs, chunk=chunk)
+                clocks=clk.summary(), launches=2 * args.steps, h2d_gbs=h2d_gbs, chunk=chunk,
+                split=split_plan)
 
 
 def save_arm(args):
@@ -452,9 +490,11 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=30, help="0 skips the end-to-end leg")
     ap.add_argument("--e2e-chunk", type=int, default=4, help="layers per streamed chunk")
     ap.add_argument("--e2e-slots", type=int, default=3, help="staging ring slots")
-    ap.add_argument("--e2e-source", default="layers", choices=["layers", "chunks"],
-                    help="host form of the hidden states: [layer][token][d], or the saved "
-                         "chunk store")
+    ap.add_argument("--e2e-source", default="layers", choices=["layers", "chunks", "split"],
+                    help="host form of the saved state: [layer][token][d] hidden states, the "
+                         "saved chunk store, or the planned split of hidden states and K/V")
+    ap.add_argument("--split-layer", type=int, default=-1,
+                    help="with --e2e-source split: first K/V layer (default: the planner's)")
     ap.add_argument("--e2e-chunk-tokens", type=int, default=64, help="tokens per saved chunk")
     ap.add_argument("--variant", type=int, default=0,
                     help="project kernel tiles: 0 automatic, 1 single CTAs, 2 CTA pairs")
@@ -576,11 +616,14 @@ def main():
                  "unit": "tokens/s",
                  "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": 4,
                  "ms_per_step": res["e2e_s"] * 1e3,
-                 "api": (f"hcr_restore_streamed, {res['chunk']}-layer chunks, "
-                         if args.e2e_source == "layers" else
-                         f"hcr_restore_streamed_chunks from a pinned host store of "
-                         f"{args.e2e_chunk_tokens}-token chunks, {res['chunk']}-layer groups, ")
-                        + f"{args.e2e_slots}-slot staging ring",
+                 "api": {"layers": f"hcr_restore_streamed, {res['chunk']}-layer chunks, ",
+                         "chunks": f"hcr_restore_streamed_chunks from a pinned host store of "
+                                   f"{args.e2e_chunk_tokens}-token chunks, {res['chunk']}-layer "
+                                   "groups, ",
+                         "split": f"hcr_restore_streamed_split (hidden states below the split, "
+                                  f"saved K/V above), {res['chunk']}-layer groups, "}[
+                            args.e2e_source] + f"{args.e2e_slots}-slot staging ring",
+                 "layer_split": res["split"],
                  "plain_h2d_gbs": res["h2d_gbs"]}
                 if res["e2e_s"] == res["e2e_s"] else None),
         "gpu_launches": res["launches"],

@@ -342,8 +342,11 @@ hcr_status hcr_save_kv(hcr_handle* h, void* kv, int32_t layer_begin, int32_t lay
  *
  * hcr_profile_layer_costs measures the four costs on the current GPU for
  * n_tokens tokens, restoring groups of layers_per_chunk layers as the
- * streamed restore does, with CUDA events on `stream` (mean of `reps` runs
- * after `reps` warm-up runs).  It allocates device and pinned host buffers
+ * streamed restore does, with CUDA events on `stream`.  The GPU costs come
+ * from restores and placements run back to back -- half a second of warm-up
+ * (at least `reps` rounds), then the mean of `reps` rounds -- so they are
+ * those of a GPU under sustained load (a power-capped GPU clocks down under
+ * sustained tensor work); the copy costs from `reps` copies of each kind.  It allocates device and pinned host buffers
  * for one group (freed before it returns) and synchronises `stream`.
  */
 typedef struct {

@@ -17,10 +17,12 @@
 // more host memory).  It reads no device state.
 //
 // hcr_profile_layer_costs measures those four per-layer costs on this GPU
-// for a token count: it restores one group of layers from device-resident
-// hidden states, places the same layers' K/V, and times host-to-device copies
-// of both, with CUDA events on the caller's stream, averaged over `reps`
-// runs after as many warm-up runs.  It allocates (and frees) its own buffers
+// for a token count, with CUDA events on the caller's stream.  GPU phase: it
+// restores one group of layers from device-resident hidden states and places
+// the same layers' K/V, alternately and back to back -- half a second of
+// warm-up (at least `reps` rounds), then `reps` timed rounds -- so the costs
+// are those of a GPU under sustained load, at the clocks a long restore runs
+// at.  Copy phase: `reps` timed host-to-device copies of both kinds.  It allocates (and frees) its own buffers
 // and fills the hidden states with a counter-based pseudo-random pattern so
 // that the tensor cores see realistic operand switching.
 #include <cuda_bf16.h>
@@ -180,67 +182,97 @@ extern "C" hcr_status hcr_profile_layer_costs(hcr_handle* h, int32_t n_tokens,
     return set_last_error(HCR_ERR_CUDA, "profiling setup: %s", cudaGetErrorString(e));
   }
   const hcr_cache_layout layout{num_blocks, kB, 0};
+  auto cuda_err = [&](const char* what) {
+    cudaGetLastError();
+    return set_last_error(HCR_ERR_CUDA, "profiling %s: %s", what, cudaGetErrorString(e));
+  };
+  // Two ops per phase: GPU work (restore, place) back to back, then copies.
+  auto gpu_op = [&](int op) -> hcr_status {
+    const int32_t* c = static_cast<int32_t*>(dcu);
+    const int32_t* st = static_cast<int32_t*>(dstart);
+    const int32_t* tb = static_cast<int32_t*>(dtable);
+    return op == 0 ? hcr_restore(h, hidden, 0, nl, n_req, n_tokens, c, st, tb, max_blocks, kc,
+                                 vc, &layout, ws, ws_bytes, stream)
+                   : hcr_load_kv(h, kv, 0, nl, n_req, n_tokens, c, st, tb, max_blocks, kc, vc,
+                                 &layout, ws, ws_bytes, stream);
+  };
+  auto copy_op = [&](int op) -> cudaError_t {
+    return op == 0 ? cudaMemcpyAsync(scratch, hh, hid_bytes, cudaMemcpyHostToDevice, s)
+                   : cudaMemcpyAsync(scratch, hkv, kv_bytes, cudaMemcpyHostToDevice, s);
+  };
   Events ev;
-  const int kOps = 4;   // restore, place, hidden copy, K/V copy
-  for (int i = 0; i < 2 * kOps * reps && e == cudaSuccess; ++i) {
+  for (int i = 0; i < 4 * reps + 2 && e == cudaSuccess; ++i) {
     cudaEvent_t x;
     e = cudaEventCreate(&x);
     if (e == cudaSuccess) ev.ev.push_back(x);
   }
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return set_last_error(HCR_ERR_CUDA, "profiling events: %s", cudaGetErrorString(e));
-  }
-  auto run = [&](int rep, bool timed) -> hcr_status {
-    for (int op = 0; op < kOps; ++op) {
-      cudaEvent_t* pair = timed ? &ev.ev[size_t(2) * (rep * kOps + op)] : nullptr;
-      if (pair && (e = cudaEventRecord(pair[0], s)) != cudaSuccess) break;
-      hcr_status st = HCR_OK;
-      if (op == 0)
-        st = hcr_restore(h, hidden, 0, nl, n_req, n_tokens, static_cast<int32_t*>(dcu),
-                         static_cast<int32_t*>(dstart), static_cast<int32_t*>(dtable),
-                         max_blocks, kc, vc, &layout, ws, ws_bytes, stream);
-      else if (op == 1)
-        st = hcr_load_kv(h, kv, 0, nl, n_req, n_tokens, static_cast<int32_t*>(dcu),
-                         static_cast<int32_t*>(dstart), static_cast<int32_t*>(dtable),
-                         max_blocks, kc, vc, &layout, ws, ws_bytes, stream);
-      else if (op == 2)
-        e = cudaMemcpyAsync(scratch, hh, hid_bytes, cudaMemcpyHostToDevice, s);
-      else
-        e = cudaMemcpyAsync(scratch, hkv, kv_bytes, cudaMemcpyHostToDevice, s);
-      if (st != HCR_OK) return st;
-      if (e != cudaSuccess) break;
-      if (pair && (e = cudaEventRecord(pair[1], s)) != cudaSuccess) break;
-    }
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return set_last_error(HCR_ERR_CUDA, "profiling run: %s", cudaGetErrorString(e));
-    }
-    return HCR_OK;
+  if (e != cudaSuccess) return cuda_err("events");
+  // events: [0, 2*reps) GPU ops (restore, place per rep), [2*reps, 4*reps)
+  // copies, and the last two bracket the first GPU round for the warm-up.
+  auto elapsed = [&](size_t i0, size_t i1, double* ms) -> bool {
+    float f = 0.f;
+    e = cudaEventElapsedTime(&f, ev.ev[i0], ev.ev[i1]);
+    *ms = f;
+    return e == cudaSuccess;
   };
+  const size_t w0 = size_t(4) * reps, w1 = w0 + 1;
+  hcr_status st = HCR_OK;
+  // GPU phase.  Warm up for at least kWarmSeconds of uninterrupted work so
+  // the clocks settle where a long restore runs them (a power-capped GPU
+  // clocks down under sustained tensor work), then time `reps` rounds with
+  // nothing else in between.
+  constexpr double kWarmSeconds = 0.5;
+  if ((e = cudaEventRecord(ev.ev[w0], s)) != cudaSuccess) return cuda_err("event record");
+  if ((st = gpu_op(0)) != HCR_OK || (st = gpu_op(1)) != HCR_OK) return st;
+  if ((e = cudaEventRecord(ev.ev[w1], s)) != cudaSuccess) return cuda_err("event record");
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_err("sync");
+  double round_ms = 0.0;
+  if (!elapsed(w0, w1, &round_ms)) return cuda_err("timing");
+  const int warm = int(std::min<double>(
+      20000.0, std::max<double>(reps, std::ceil(kWarmSeconds * 1e3 / std::max(round_ms, 1e-3)))));
+  for (int r = 0; r < warm; ++r)
+    if ((st = gpu_op(0)) != HCR_OK || (st = gpu_op(1)) != HCR_OK) return st;
   for (int r = 0; r < reps; ++r) {
-    hcr_status st = run(r, false);
-    if (st != HCR_OK) return st;
+    // consecutive events: rep r's restore is [2r, 2r+1), its placement [2r+1, 2r+2)
+    if ((e = cudaEventRecord(ev.ev[size_t(2) * r], s)) != cudaSuccess)
+      return cuda_err("event record");
+    if ((st = gpu_op(0)) != HCR_OK) return st;
+    if ((e = cudaEventRecord(ev.ev[size_t(2) * r + 1], s)) != cudaSuccess)
+      return cuda_err("event record");
+    if ((st = gpu_op(1)) != HCR_OK) return st;
   }
-  for (int r = 0; r < reps; ++r) {
-    hcr_status st = run(r, true);
-    if (st != HCR_OK) return st;
-  }
-  uint32_t flags = 0;
-  hcr_status st = hcr_check_device_error(h, stream, &flags);   // synchronises the stream
-  if (st != HCR_OK) return st;
-  double sum[kOps] = {0, 0, 0, 0};
+  if ((e = cudaEventRecord(ev.ev[w0], s)) != cudaSuccess) return cuda_err("event record");
+  // Copy phase: one untimed round, then `reps` timed rounds.
+  for (int op = 0; op < 2; ++op)
+    if ((e = copy_op(op)) != cudaSuccess) return cuda_err("copy");
   for (int r = 0; r < reps; ++r)
-    for (int op = 0; op < kOps; ++op) {
-      float ms = 0.f;
-      e = cudaEventElapsedTime(&ms, ev.ev[size_t(2) * (r * kOps + op)],
-                               ev.ev[size_t(2) * (r * kOps + op) + 1]);
-      if (e != cudaSuccess) {
-        cudaGetLastError();
-        return set_last_error(HCR_ERR_CUDA, "profiling timing: %s", cudaGetErrorString(e));
-      }
-      sum[op] += ms;
+    for (int op = 0; op < 2; ++op) {
+      const size_t i = size_t(2) * reps + size_t(2) * r + op;
+      if ((e = cudaEventRecord(ev.ev[i], s)) != cudaSuccess) return cuda_err("event record");
+      if ((e = copy_op(op)) != cudaSuccess) return cuda_err("copy");
     }
+  if ((e = cudaEventRecord(ev.ev[w1], s)) != cudaSuccess) return cuda_err("event record");
+  uint32_t flags = 0;
+  st = hcr_check_device_error(h, stream, &flags);   // synchronises the stream
+  if (st != HCR_OK) return st;
+  double sum[4] = {0, 0, 0, 0};   // restore, place, hidden copy, K/V copy
+  for (int r = 0; r < reps; ++r) {
+    double ms = 0.0;
+    const size_t g = size_t(2) * r;
+    // the end of rep r's placement is the start of rep r+1's restore, or the
+    // event recorded after the GPU phase
+    const size_t g_end = r + 1 < reps ? g + 2 : w0;
+    if (!elapsed(g, g + 1, &ms)) return cuda_err("timing");
+    sum[0] += ms;
+    if (!elapsed(g + 1, g_end, &ms)) return cuda_err("timing");
+    sum[1] += ms;
+    const size_t c = size_t(2) * reps + g;
+    const size_t c_end = r + 1 < reps ? c + 2 : w1;
+    if (!elapsed(c, c + 1, &ms)) return cuda_err("timing");
+    sum[2] += ms;
+    if (!elapsed(c + 1, c_end, &ms)) return cuda_err("timing");
+    sum[3] += ms;
+  }
   const double per = 1e-3 / (double(reps) * nl);   // ms over reps and layers -> s per layer
   out->restore_s = sum[0] * per;
   out->kv_place_s = sum[1] * per;

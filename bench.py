@@ -343,10 +343,12 @@ def gpu_arm(args, rank, world, local_rank):
                                               ("restore_s", "hidden_copy_s", "kv_copy_s",
                                                "kv_place_s")})
     t0 = time.perf_counter()
+    step_s = []
     for i in range(2 + e2e_steps if e2e_steps > 0 else 0):
         if i == 2:
             torch.cuda.synchronize(device)
             t0 = time.perf_counter()
+        ts = time.perf_counter()
         for hm, dm in zip(meta_host, meta_dev):
             dm.copy_(hm, non_blocking=True)
         if split_plan is not None:
@@ -368,6 +370,8 @@ def gpu_arm(args, rank, world, local_rank):
         st, _ = r.check(stream)          # syncs and reads the 4-byte status word
         if st != 0:
             raise RuntimeError("device error in e2e leg")
+        if i >= 2:
+            step_s.append(time.perf_counter() - ts)
     e2e_s = (time.perf_counter() - t0) / e2e_steps if e2e_steps > 0 else float("nan")
     # context: one plain copy of all hidden states, host to device
     h2d_gbs = None
@@ -380,11 +384,13 @@ def gpu_arm(args, rank, world, local_rank):
         h2d_gbs = hidden_host.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9
 
     t_step = total_ms / 1e3 / args.steps
-    t_step, proj_ms, prep_ms, e2e_s = reduce_max_over_ranks([t_step, proj_ms, prep_ms, e2e_s],
-                                                            device)
+    e2e_med = statistics.median(step_s) if step_s else float("nan")
+    t_step, proj_ms, prep_ms, e2e_s, e2e_med = reduce_max_over_ranks(
+        [t_step, proj_ms, prep_ms, e2e_s, e2e_med], device)
     return dict(w=w, t_step=t_step, proj_ms=proj_ms, prep_ms=prep_ms, e2e_s=e2e_s, h2d=h2d,
                 clocks=clk.summary(), launches=2 * args.steps, h2d_gbs=h2d_gbs, chunk=chunk,
-                split=split_plan)
+                split=split_plan,
+                e2e_median_s=e2e_med)
 
 
 def save_arm(args):
@@ -616,6 +622,7 @@ def main():
                  "unit": "tokens/s",
                  "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": 4,
                  "ms_per_step": res["e2e_s"] * 1e3,
+                 "ms_per_step_median": res["e2e_median_s"] * 1e3,
                  "api": {"layers": f"hcr_restore_streamed, {res['chunk']}-layer chunks, ",
                          "chunks": f"hcr_restore_streamed_chunks from a pinned host store of "
                                    f"{args.e2e_chunk_tokens}-token chunks, {res['chunk']}-layer "

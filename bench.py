@@ -189,8 +189,12 @@ def oracle_child(args):
                       "value": rows / (t * s.n_layers)}))
 
 
-def run_oracle(workload: str, rows: int, seconds: float, max_reps: int, warmup: int = 0):
+def run_oracle(workload: str, rows: int, seconds: float, max_reps: int, warmup: int = 0,
+               threads: int = 0):
+    """threads = 0: all of this process's cores."""
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    if threads:
+        cores = min(cores, threads)
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = str(cores)
@@ -603,6 +607,11 @@ def main():
         cpu = {"value": o["value"], "unit": "tokens/s", "cores": o["cores"], "kind": "oracle",
                "sample": f"1 layer x {o['rows']} tokens of the {w.name} workload, "
                          f"{o['reps']} reps (mean), extrapolated to all {s.n_layers} layers"}
+        o1 = run_oracle(args.workload, min(args.oracle_rows, 1024), args.oracle_seconds / 3,
+                        args.oracle_max_reps, threads=1)
+        cpu["single_thread"] = {"value": o1["value"], "cores": 1,
+                                "sample": f"1 layer x {o1['rows']} tokens, {o1['reps']} reps "
+                                          f"(mean), extrapolated to {s.n_layers} layers"}
     line = {
         "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,

@@ -222,10 +222,22 @@ hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
   p.head_dim = d.head_dim;
   p.n_layers = nl;
   p.layer_begin = a.layer_begin;
-  // CTA pairs (256-row tiles) once there is more than one 128-row tile of
-  // tokens; single CTAs for short restores, which stream weights from HBM
-  // and would only pad the pair's second half.
-  bool pair = H.pair_clusters > 0 && a.n_tokens > kBlockM;
+  // Tile variant, chosen from measurements on GB300:
+  //   * CTA pairs (256-row tiles) once there is more than one 128-row tile of
+  //     tokens: they do ~8-12% more work per clock, and weight-streaming
+  //     restores of 129-256 tokens run ~15% faster with them;
+  //   * single CTAs for short restores (one 128-row tile of tokens), which
+  //     would only pad the pair's second half;
+  //   * single CTAs where 128-row tiles pad at least 10% fewer rows than
+  //     256-row tiles (e.g. 300, 640 or 794 tokens): the padding saved
+  //     outweighs the lower rate;
+  //   * single CTAs for models wider than 4096: at d_model 5120 and 7168 they
+  //     ran 4-5% faster in long power-capped restores and no slower at
+  //     2-4K tokens, while at 4096 pairs win by 5-7%.
+  const int64_t pad256 = (int64_t(a.n_tokens) + 2 * kBlockM - 1) / (2 * kBlockM) * (2 * kBlockM);
+  const int64_t pad128 = (int64_t(a.n_tokens) + kBlockM - 1) / kBlockM * kBlockM;
+  bool pair = H.pair_clusters > 0 && a.n_tokens > kBlockM && d.d_model <= 4096 &&
+              10 * pad128 > 9 * pad256;
   if (H.variant == 1) pair = false;
   if (H.variant == 2) pair = H.pair_clusters > 0;
   const int tile_m = pair ? 2 * kBlockM : kBlockM;

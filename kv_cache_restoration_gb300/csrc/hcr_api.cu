@@ -169,6 +169,7 @@ hcr_status validate_restore(const hcr_handle* h, const RestoreArgs& a, bool* emp
 
 // stats = false: the slot map only (the K/V row copies need no statistics).
 hcr_status do_prepare(hcr_handle* h, const RestoreArgs& a, bool stats = true) {
+  NvtxRange range("hcr.prepare");
   const Handle& H = h->impl;
   const hcr_model_dims& d = H.dims;
   const int32_t nl = stats ? a.layer_end - a.layer_begin : 0;
@@ -202,6 +203,7 @@ hcr_status do_prepare(hcr_handle* h, const RestoreArgs& a, bool stats = true) {
 }
 
 hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
+  NvtxRange range("hcr.project");
   const Handle& H = h->impl;
   const hcr_model_dims& d = H.dims;
   const int32_t nl = a.layer_end - a.layer_begin;
@@ -486,6 +488,7 @@ hcr_status hcr_restore(hcr_handle* h, const void* hidden, int32_t layer_begin, i
                        int32_t max_blocks_per_req, void* k_cache, void* v_cache,
                        const hcr_cache_layout* layout, void* workspace, size_t workspace_bytes,
                        void* stream) {
+  NvtxRange range("hcr_restore");
   HCR_RESTORE_ARGS;
   bool empty = false;
   hcr_status st = validate_restore(h, a, &empty);
@@ -496,6 +499,7 @@ hcr_status hcr_restore(hcr_handle* h, const void* hidden, int32_t layer_begin, i
 }
 
 static hcr_status kv_rows(hcr_handle* h, const RestoreArgs& a, bool to_cache, const char* what) {
+  NvtxRange range(to_cache ? "hcr_load_kv" : "hcr_save_kv");
   bool empty = false;
   hcr_status st = validate_restore(h, a, &empty, /*stats=*/false);
   if (st != HCR_OK || empty) return st;

@@ -8,6 +8,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/hcr.h"
 
 namespace hcr {
@@ -156,6 +158,16 @@ struct KvRowsParams {
   int64_t layer_stride_vecs;
   int32_t row_vecs;        // n_kv_heads * head_dim / 8
   int32_t n_tokens, n_layers;
+};
+
+// An NVTX range on the calling host thread for the scope's lifetime: the
+// library's entry points and stages show up by name in a timeline profiler
+// (nothing is recorded when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
 // Records a message for hcr_last_error() on this host thread; returns s.

@@ -122,6 +122,7 @@ extern "C" hcr_status hcr_plan_layer_split(const hcr_layer_costs* c, int32_t n_l
 extern "C" hcr_status hcr_profile_layer_costs(hcr_handle* h, int32_t n_tokens,
                                               int32_t layers_per_chunk, int32_t reps,
                                               void* stream, hcr_layer_costs* out) {
+  NvtxRange range("hcr_profile_layer_costs");
   if (!h || !out) return set_last_error(HCR_ERR_INVALID_ARG, "handle and out must be non-NULL");
   if (n_tokens < 1 || layers_per_chunk < 1 || reps < 1)
     return set_last_error(HCR_ERR_INVALID_ARG,

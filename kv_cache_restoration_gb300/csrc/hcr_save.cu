@@ -133,6 +133,7 @@ extern "C" hcr_status hcr_save_hidden(hcr_handle* h, const void* hidden, int32_t
                                       const int32_t* chunk_table, int32_t max_chunks_per_req,
                                       int32_t chunk_tokens, void* chunk_store,
                                       int32_t num_chunks, void* stream) {
+  NvtxRange range("hcr_save_hidden");
   if (!h) return set_last_error(HCR_ERR_INVALID_ARG, "handle is NULL");
   const hcr_model_dims& d = h->impl.dims;
   if (layer_begin < 0 || layer_end < layer_begin || layer_end > d.n_layers)

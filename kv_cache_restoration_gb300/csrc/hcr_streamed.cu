@@ -93,6 +93,7 @@ hcr_status run_pipeline(hcr_handle* h, const std::vector<Item>& items, size_t sl
                         void* v_cache, const hcr_cache_layout* layout, void* staging,
                         size_t staging_bytes, size_t workspace_need, void* workspace,
                         size_t workspace_bytes, void* stream, const CopyFn& copy_item) {
+  NvtxRange range("hcr.streamed_pipeline");
   const hcr_model_dims& d = h->impl.dims;
   if (!layout) return set_last_error(HCR_ERR_INVALID_ARG, "layout is NULL");
   if (!staging || reinterpret_cast<uintptr_t>(staging) % 256)
@@ -132,7 +133,10 @@ hcr_status run_pipeline(hcr_handle* h, const std::vector<Item>& items, size_t sl
     if (c >= size_t(slots) &&
         (e = cudaStreamWaitEvent(r->copy, r->done[slot], 0)) != cudaSuccess)
       return cuda_err(e, "stream wait");
-    if ((e = copy_item(it, dst, r->copy)) != cudaSuccess) return cuda_err(e, "host copy");
+    {
+      NvtxRange copy_range(it.kv ? "hcr.copy_kv_group" : "hcr.copy_hidden_group");
+      if ((e = copy_item(it, dst, r->copy)) != cudaSuccess) return cuda_err(e, "host copy");
+    }
     if ((e = cudaEventRecord(r->copied[slot], r->copy)) != cudaSuccess)
       return cuda_err(e, "event record");
     if ((e = cudaStreamWaitEvent(s, r->copied[slot], 0)) != cudaSuccess)

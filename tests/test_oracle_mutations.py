@@ -281,3 +281,102 @@ def test_planted_split_mistake_is_caught(monkeypatch, attr, mutant):
         except (AssertionError, ValueError, IndexError):
             failed += 1
     assert failed, f"no pin caught {mutant.__name__}"
+
+
+# ----------------------------------------------------------------------------- codec
+from oracle import codec as CK  # noqa: E402
+from tests import test_oracle_codec as TCK  # noqa: E402
+
+CODEC_ORIG = {n: getattr(CK, n) for n in ("encode_layer", "group_anchors", "layer_bin",
+                                          "quantise_anchor", "rint32", "decode_layer")}
+
+
+def _encode_open_loop(h, anchors, b):
+    # mistake: delta from the original anchor row, not the decoded one
+    codes, scales = CODEC_ORIG["encode_layer"](h, anchors, b)
+    h = np.asarray(h, np.float32)
+    for t in range(len(h)):
+        if anchors[t] != t:
+            d = (h[t] - h[anchors[t]]).astype(np.float32)
+            codes[t] = np.clip(np.rint(d / np.float32(b)), -127, 127).astype(np.int8)
+    return codes, scales
+
+
+def _encode_chained(h, anchors, b):
+    # mistake: each delta from the previous token's decoded row
+    codes, scales = CODEC_ORIG["encode_layer"](h, anchors, b)
+    h = np.asarray(h, np.float32)
+    prev = None
+    for t in range(len(h)):
+        if anchors[t] == t:
+            prev = CK.dequantise_anchor(codes[t], scales[t])
+            continue
+        d = (h[t] - prev).astype(np.float32)
+        codes[t] = np.clip(np.rint(d / np.float32(b)), -127, 127).astype(np.int8)
+        prev = (prev + codes[t].astype(np.float32) * np.float32(b)).astype(np.float32)
+    return codes, scales
+
+
+def _anchors_ignore_requests(cu_seqlens, group_tokens=10):
+    T = int(np.asarray(cu_seqlens)[-1])
+    return (np.arange(T) // group_tokens) * group_tokens
+
+
+def _bins_reversed(layer, n_layers, bins=CK.DEFAULT_BINS):
+    return np.float32(bins[2 - min(2, (3 * layer) // n_layers)])
+
+
+def _bins_by_thirds_rounded(layer, n_layers, bins=CK.DEFAULT_BINS):
+    return np.float32(bins[min(2, round(3 * layer / n_layers))])
+
+
+def _anchor_255(h):
+    h = np.asarray(h, np.float32)
+    m = np.float32(np.max(np.abs(h)))
+    s = np.float32(m / np.float32(255))
+    if s == 0:
+        return np.zeros(h.shape, np.int8), np.float32(0)
+    return np.clip(np.rint(h / s), -127, 127).astype(np.int8), s
+
+
+def _round_half_away(x):
+    x = np.asarray(x, np.float32)
+    return (np.sign(x) * np.floor(np.abs(x) + np.float32(0.5))).astype(np.float32)
+
+
+def _decode_plain_code(codes, scales, anchors, b):
+    # mistake: a delta row decodes to c * b without the anchor
+    out = CODEC_ORIG["decode_layer"](codes, scales, anchors, b)
+    for t in range(len(out)):
+        if anchors[t] != t:
+            out[t] = codes[t].astype(np.float32) * np.float32(b)
+    return out
+
+
+CODEC_PINS = [TCK.test_hand_worked_group, TCK.test_group_boundaries_by_request,
+              lambda: TCK.test_group_anchors_brute_force(1), TCK.test_layer_group_rule_by_hand,
+              lambda: TCK.test_error_bounds(0.5), TCK.test_lossless_when_values_sit_on_the_grids,
+              TCK.test_saturation_and_zero_rows, TCK.test_groups_decode_independently,
+              TCK.test_multi_layer_encode_uses_each_layers_bin]
+
+
+@pytest.mark.parametrize("attr,mutant", [("encode_layer", _encode_open_loop),
+                                         ("encode_layer", _encode_chained),
+                                         ("group_anchors", _anchors_ignore_requests),
+                                         ("layer_bin", _bins_reversed),
+                                         ("layer_bin", _bins_by_thirds_rounded),
+                                         ("quantise_anchor", _anchor_255),
+                                         ("rint32", _round_half_away),
+                                         ("decode_layer", _decode_plain_code)],
+                         ids=["open_loop", "chained", "groups_cross_requests", "bins_reversed",
+                              "bins_rounded", "anchor_255", "round_half_away",
+                              "decode_without_anchor"])
+def test_planted_codec_mistake_is_caught(monkeypatch, attr, mutant):
+    monkeypatch.setattr(CK, attr, mutant)
+    failed = 0
+    for pin in CODEC_PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            failed += 1
+    assert failed, f"no pin caught {mutant.__name__}"

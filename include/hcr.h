@@ -395,6 +395,70 @@ hcr_status hcr_restore_streamed_split(hcr_handle* h, const void* hidden_host,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Hidden-state codec (HCache episode, cues 30 and 32: quantise hidden states
+ * the way CacheGen quantises KV; CacheGen review, section 核心方法: groups of
+ * 10 tokens with an 8-bit anchor and deltas from it, quantised with bins of
+ * 0.5 / 1 / 1.5 for the first / middle / last third of the layers).  The
+ * page's lossless arithmetic-coding stage is not part of this library.
+ *
+ *   groups:  token i of a request belongs to the group whose anchor is token
+ *            group_tokens * (i / group_tokens) of the same request;
+ *   anchor:  s = max|h| / 127 (float32), q = rint(h / s) in [-127, 127]
+ *            (all 0 when s = 0); decoded q * s;
+ *   others:  c = rint((h - q s) / b) in [-127, 127]; decoded q s + c b, with
+ *            b = bins[min(2, 3 l / n_layers)] for model layer l;
+ *   every step one IEEE binary32 operation rounded to nearest even; the
+ *   decoded value rounded once to the storage dtype.
+ *
+ * Encoded form: codes int8 [layer_end - layer_begin][n_tokens][d_model] and
+ * scales float32 [layer_end - layer_begin][n_tokens] (anchor rows only; other
+ * entries are not written).  Codes and scales may be device memory or pinned
+ * (mapped) host memory; hidden must be device memory, 16-byte aligned;
+ * codes 8-byte and scales 4-byte aligned.  cu_seqlens is a device array as
+ * in hcr_restore.  Each call enqueues one kernel on `stream`; a token in no
+ * request (cu_seqlens inconsistent with n_tokens) is skipped and flagged
+ * HCR_DEVERR_SEQLENS.  Bins must be finite and > 0, group_tokens >= 1.
+ */
+typedef struct {
+  float bins[3];          /* delta bins for the first, middle, last third of the layers */
+  int32_t group_tokens;   /* tokens per anchor group (10 on the page)                     */
+} hcr_codec_params;
+
+hcr_status hcr_encode_hidden(hcr_handle* h, const hcr_codec_params* params, const void* hidden,
+                             int32_t layer_begin, int32_t layer_end, int32_t n_req,
+                             int32_t n_tokens, const int32_t* cu_seqlens, void* codes,
+                             void* scales, void* stream);
+hcr_status hcr_decode_hidden(hcr_handle* h, const hcr_codec_params* params, const void* codes,
+                             const void* scales, int32_t layer_begin, int32_t layer_end,
+                             int32_t n_req, int32_t n_tokens, const int32_t* cu_seqlens,
+                             void* hidden, void* stream);
+
+/*
+ * hcr_restore_streamed_encoded -- hcr_restore_streamed from the codec's
+ * encoded form in pinned host memory:
+ *     codes_host  [layer_end - layer_begin][n_tokens][d_model] int8
+ *     scales_host [layer_end - layer_begin][n_tokens] float32
+ * as hcr_encode_hidden writes them (with the same params).  Each group of
+ * layers_per_chunk layers is copied (about half the bytes of the hidden
+ * states), decoded on `stream` into a decode buffer, then restored.  The
+ * caches are bit-identical to hcr_restore of hcr_decode_hidden's output.
+ * staging (256-byte aligned) holds the decode buffer, align256(chunk * n_tokens
+ * * d_model * 2) bytes, then the slots, each align256(chunk * n_tokens *
+ * d_model) + align256(chunk * n_tokens * 4) bytes (up to 8 are used).  Other
+ * arguments and behaviour are as in hcr_restore_streamed.
+ */
+hcr_status hcr_restore_streamed_encoded(hcr_handle* h, const hcr_codec_params* params,
+                                        const void* codes_host, const void* scales_host,
+                                        int32_t layer_begin, int32_t layer_end, int32_t n_req,
+                                        int32_t n_tokens, const int32_t* cu_seqlens,
+                                        const int32_t* start_pos, const int32_t* block_table,
+                                        int32_t max_blocks_per_req, void* k_cache,
+                                        void* v_cache, const hcr_cache_layout* layout,
+                                        void* staging, size_t staging_bytes,
+                                        int32_t layers_per_chunk, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
+/*
  * hcr_restore_no_alloc -- hcr_restore without a caller-provided workspace.
  *
  * The paper has no counterpart to this call; it exists for callers of this

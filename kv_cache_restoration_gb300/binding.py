@@ -65,6 +65,14 @@ class hcr_layer_split(ctypes.Structure):
                 ("predicted_s", ctypes.c_double)]
 
 
+class hcr_codec_params(ctypes.Structure):
+    _fields_ = [("bins", ctypes.c_float * 3), ("group_tokens", ctypes.c_int32)]
+
+
+def codec_params(bins=(0.5, 1.0, 1.5), group_tokens: int = 10) -> hcr_codec_params:
+    return hcr_codec_params((ctypes.c_float * 3)(*bins), group_tokens)
+
+
 class HcrError(RuntimeError):
     def __init__(self, status: int, where: str, message: str):
         super().__init__(f"{where}: {message}")
@@ -118,6 +126,17 @@ lib.hcr_restore_streamed_split.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32
                                            _vp, _i32, _vp, _vp, ctypes.POINTER(hcr_cache_layout),
                                            _vp, ctypes.c_size_t, _i32, _vp, ctypes.c_size_t, _vp]
 lib.hcr_restore_streamed_split.restype = ctypes.c_int
+lib.hcr_encode_hidden.argtypes = [_vp, ctypes.POINTER(hcr_codec_params), _vp, _i32, _i32, _i32,
+                                  _i32, _vp, _vp, _vp, _vp]
+lib.hcr_encode_hidden.restype = ctypes.c_int
+lib.hcr_decode_hidden.argtypes = [_vp, ctypes.POINTER(hcr_codec_params), _vp, _vp, _i32, _i32,
+                                  _i32, _i32, _vp, _vp, _vp]
+lib.hcr_decode_hidden.restype = ctypes.c_int
+lib.hcr_restore_streamed_encoded.argtypes = [_vp, ctypes.POINTER(hcr_codec_params), _vp, _vp,
+                                             _i32, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _vp,
+                                             _vp, ctypes.POINTER(hcr_cache_layout), _vp,
+                                             ctypes.c_size_t, _i32, _vp, ctypes.c_size_t, _vp]
+lib.hcr_restore_streamed_encoded.restype = ctypes.c_int
 lib.hcr_restore_no_alloc.argtypes = _RESTORE_ARGTYPES[:13] + [_vp]
 lib.hcr_restore_no_alloc.restype = ctypes.c_int
 HCR_NO_ALLOC_SCRATCH_BYTES = 16 << 20
@@ -318,6 +337,55 @@ def hcr_restore_streamed_split(handle, hidden_host, kv_host, layer_begin, split_
         _stream_ptr(stream))
     if check:
         _check(st, "hcr_restore_streamed_split")
+    return st
+
+
+def hcr_encode_hidden(handle, params: hcr_codec_params, hidden, layer_begin, layer_end, n_req,
+                      n_tokens, cu_seqlens, codes, scales, stream=None, *,
+                      check: bool = True) -> int:
+    """Anchor + delta codec: hidden [layers][tokens][d] -> int8 codes + float32 scales."""
+    st = lib.hcr_encode_hidden(handle, ctypes.byref(params), _ptr(hidden), layer_begin,
+                               layer_end, n_req, n_tokens, _ptr(cu_seqlens), _ptr(codes),
+                               _ptr(scales), _stream_ptr(stream))
+    if check:
+        _check(st, "hcr_encode_hidden")
+    return st
+
+
+def hcr_decode_hidden(handle, params: hcr_codec_params, codes, scales, layer_begin, layer_end,
+                      n_req, n_tokens, cu_seqlens, hidden, stream=None, *,
+                      check: bool = True) -> int:
+    """Inverse of hcr_encode_hidden, into the storage dtype."""
+    st = lib.hcr_decode_hidden(handle, ctypes.byref(params), _ptr(codes), _ptr(scales),
+                               layer_begin, layer_end, n_req, n_tokens, _ptr(cu_seqlens),
+                               _ptr(hidden), _stream_ptr(stream))
+    if check:
+        _check(st, "hcr_decode_hidden")
+    return st
+
+
+def encoded_staging_bytes(n_tokens: int, d_model: int, layers_per_chunk: int, slots: int) -> int:
+    """Staging hcr_restore_streamed_encoded needs: the decode buffer plus `slots` slots."""
+    def a(x):
+        return (x + 255) // 256 * 256
+    c = layers_per_chunk
+    return a(c * n_tokens * d_model * 2) + slots * (a(c * n_tokens * d_model) + a(c * n_tokens * 4))
+
+
+def hcr_restore_streamed_encoded(handle, params: hcr_codec_params, codes_host, scales_host,
+                                 layer_begin, layer_end, n_req, n_tokens, cu_seqlens, start_pos,
+                                 block_table, max_blocks_per_req, k_cache, v_cache, layout,
+                                 staging, staging_bytes, layers_per_chunk, workspace,
+                                 workspace_bytes, stream=None, *, check: bool = True) -> int:
+    """Layer-pipelined restore from the codec's encoded form in host memory."""
+    st = lib.hcr_restore_streamed_encoded(
+        handle, ctypes.byref(params), _ptr(codes_host), _ptr(scales_host), layer_begin,
+        layer_end, n_req, n_tokens, _ptr(cu_seqlens), _ptr(start_pos), _ptr(block_table),
+        max_blocks_per_req, _ptr(k_cache), _ptr(v_cache),
+        ctypes.byref(layout) if layout is not None else None, _ptr(staging), staging_bytes,
+        layers_per_chunk, _ptr(workspace), workspace_bytes, _stream_ptr(stream))
+    if check:
+        _check(st, "hcr_restore_streamed_encoded")
     return st
 
 

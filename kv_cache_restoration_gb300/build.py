@@ -20,7 +20,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhcr.so")
 
 SOURCES = ["hcr_api.cu", "hcr_prepare.cu", "hcr_project.cu", "hcr_no_alloc.cu",
-           "hcr_streamed.cu", "hcr_save.cu", "hcr_kv.cu", "hcr_plan.cu"]
+           "hcr_streamed.cu", "hcr_save.cu", "hcr_kv.cu", "hcr_plan.cu",
+           "hcr_codec.cu"]
 HEADERS = ["hcr_internal.h", "ptx.cuh"]
 
 NVCC_FLAGS = [

@@ -86,13 +86,20 @@ struct Item {
 // [nl][n_tokens][d_model], or K/V laid out [nl][2][n_tokens][d_kv].
 using CopyFn = std::function<cudaError_t(const Item& it, void* dst, cudaStream_t copy)>;
 
+// Enqueues an item's GPU work on the caller's stream once its copy has
+// landed in `src`: by default hcr_restore (hidden states) or hcr_load_kv
+// (K/V); `lb` is the item's first model layer, kc/vc its cache bases.
+using ProcessFn =
+    std::function<hcr_status(const Item& it, void* src, int32_t lb, void* kc, void* vc)>;
+
 hcr_status run_pipeline(hcr_handle* h, const std::vector<Item>& items, size_t slot_bytes,
                         int32_t layer_begin, int32_t n_req, int32_t n_tokens,
                         const int32_t* cu_seqlens, const int32_t* start_pos,
                         const int32_t* block_table, int32_t max_blocks_per_req, void* k_cache,
                         void* v_cache, const hcr_cache_layout* layout, void* staging,
                         size_t staging_bytes, size_t workspace_need, void* workspace,
-                        size_t workspace_bytes, void* stream, const CopyFn& copy_item) {
+                        size_t workspace_bytes, void* stream, const CopyFn& copy_item,
+                        const ProcessFn* process = nullptr) {
   NvtxRange range("hcr.streamed_pipeline");
   const hcr_model_dims& d = h->impl.dims;
   if (!layout) return set_last_error(HCR_ERR_INVALID_ARG, "layout is NULL");
@@ -144,12 +151,15 @@ hcr_status run_pipeline(hcr_handle* h, const std::vector<Item>& items, size_t sl
     auto* kc = static_cast<uint16_t*>(k_cache) + int64_t(it.l0) * stride;
     auto* vc = static_cast<uint16_t*>(v_cache) + int64_t(it.l0) * stride;
     const int32_t lb = layer_begin + it.l0;
-    st = it.kv ? hcr_load_kv(h, dst, lb, lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos,
-                             block_table, max_blocks_per_req, kc, vc, layout, workspace,
-                             workspace_bytes, stream)
-               : hcr_restore(h, dst, lb, lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos,
-                             block_table, max_blocks_per_req, kc, vc, layout, workspace,
-                             workspace_bytes, stream);
+    if (process)
+      st = (*process)(it, dst, lb, kc, vc);
+    else
+      st = it.kv ? hcr_load_kv(h, dst, lb, lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos,
+                               block_table, max_blocks_per_req, kc, vc, layout, workspace,
+                               workspace_bytes, stream)
+                 : hcr_restore(h, dst, lb, lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos,
+                               block_table, max_blocks_per_req, kc, vc, layout, workspace,
+                               workspace_bytes, stream);
     if (st != HCR_OK) return st;
     if ((e = cudaEventRecord(r->done[slot], s)) != cudaSuccess)
       return cuda_err(e, "event record");
@@ -366,4 +376,68 @@ extern "C" hcr_status hcr_restore_streamed_split(
         return cudaMemcpyAsync(dst, hid + size_t(it.l0) * hid_layer, size_t(it.nl) * hid_layer,
                                cudaMemcpyHostToDevice, copy);
       });
+}
+
+extern "C" hcr_status hcr_restore_streamed_encoded(
+    hcr_handle* h, const hcr_codec_params* params, const void* codes_host,
+    const void* scales_host, int32_t layer_begin, int32_t layer_end, int32_t n_req,
+    int32_t n_tokens, const int32_t* cu_seqlens, const int32_t* start_pos,
+    const int32_t* block_table, int32_t max_blocks_per_req, void* k_cache, void* v_cache,
+    const hcr_cache_layout* layout, void* staging, size_t staging_bytes,
+    int32_t layers_per_chunk, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!h) return set_last_error(HCR_ERR_INVALID_ARG, "handle is NULL");
+  const hcr_model_dims& d = h->impl.dims;
+  if (layer_begin < 0 || layer_end < layer_begin || layer_end > d.n_layers)
+    return set_last_error(HCR_ERR_INVALID_ARG, "layer range [%d, %d) outside [0, %d)",
+                          layer_begin, layer_end, d.n_layers);
+  if (n_tokens < 0) return set_last_error(HCR_ERR_INVALID_ARG, "n_tokens must be >= 0");
+  if (n_tokens == 0 || layer_end == layer_begin) return HCR_OK;
+  if (!params || !codes_host || !scales_host)
+    return set_last_error(HCR_ERR_INVALID_ARG, "params, codes_host and scales_host are needed");
+  if (layers_per_chunk < 1)
+    return set_last_error(HCR_ERR_INVALID_ARG, "layers_per_chunk must be >= 1");
+  if (!staging || reinterpret_cast<uintptr_t>(staging) % 256)
+    return set_last_error(HCR_ERR_WORKSPACE, "staging must be non-NULL and 256-byte aligned");
+  const int32_t n_layers = layer_end - layer_begin;
+  const int32_t chunk = std::min(layers_per_chunk, n_layers);
+  const size_t T = size_t(n_tokens), dm = size_t(d.d_model);
+  // staging: [decoded hidden states of one group][slot 0: codes | scales][slot 1] ...
+  const size_t decoded_bytes = align_up(size_t(chunk) * T * dm * 2, 256);
+  const size_t codes_bytes = align_up(size_t(chunk) * T * dm, 256);
+  const size_t slot_bytes = codes_bytes + align_up(size_t(chunk) * T * 4, 256);
+  if (staging_bytes < decoded_bytes + slot_bytes)
+    return set_last_error(HCR_ERR_WORKSPACE, "staging has %zu bytes; the decode buffer and "
+                          "one slot need %zu", staging_bytes, decoded_bytes + slot_bytes);
+  void* decoded = staging;
+  std::vector<Item> items;
+  for (int32_t l0 = 0; l0 < n_layers; l0 += chunk)
+    items.push_back({false, l0, std::min(chunk, n_layers - l0)});
+  const uint8_t* codes = static_cast<const uint8_t*>(codes_host);
+  const uint8_t* scales = static_cast<const uint8_t*>(scales_host);
+  // The decode of group i+1 follows the restore of group i on the caller's
+  // stream, so one decode buffer serves every group.
+  const ProcessFn decode_then_restore = [&](const Item& it, void* src, int32_t lb, void* kc,
+                                            void* vc) {
+    const uint8_t* slot = static_cast<const uint8_t*>(src);
+    hcr_status st = hcr_decode_hidden(h, params, slot, slot + codes_bytes, lb, lb + it.nl,
+                                      n_req, n_tokens, cu_seqlens, decoded, stream);
+    if (st != HCR_OK) return st;
+    return hcr_restore(h, decoded, lb, lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos,
+                       block_table, max_blocks_per_req, kc, vc, layout, workspace,
+                       workspace_bytes, stream);
+  };
+  return run_pipeline(
+      h, items, slot_bytes, layer_begin, n_req, n_tokens, cu_seqlens, start_pos, block_table,
+      max_blocks_per_req, k_cache, v_cache, layout, static_cast<uint8_t*>(staging) + decoded_bytes,
+      staging_bytes - decoded_bytes, hcr_workspace_bytes(h, n_tokens, chunk), workspace,
+      workspace_bytes, stream,
+      [&](const Item& it, void* dst, cudaStream_t copy) {
+        uint8_t* slot = static_cast<uint8_t*>(dst);
+        cudaError_t e = cudaMemcpyAsync(slot, codes + size_t(it.l0) * T * dm,
+                                        size_t(it.nl) * T * dm, cudaMemcpyHostToDevice, copy);
+        if (e != cudaSuccess) return e;
+        return cudaMemcpyAsync(slot + codes_bytes, scales + size_t(it.l0) * T * 4,
+                               size_t(it.nl) * T * 4, cudaMemcpyHostToDevice, copy);
+      },
+      &decode_then_restore);
 }

@@ -346,6 +346,21 @@ def gpu_arm(args, rank, world, local_rank):
                           costs_ms_per_layer={f: getattr(costs, f) * 1e3 for f in
                                               ("restore_s", "hidden_copy_s", "kv_copy_s",
                                                "kv_place_s")})
+    enc = None
+    if args.e2e_source == "encoded" and e2e_steps > 0:
+        # The codec's encoded form (int8 codes + anchor scales) in pinned host
+        # memory, written once by the encode kernel before the timed region.
+        params = B.codec_params()
+        codes_h = torch.empty((L, T, s.d_model), dtype=torch.int8).pin_memory()
+        scales_h = torch.zeros((L, T), dtype=torch.float32).pin_memory()
+        B.hcr_encode_hidden(r.handle, params, case.hidden, 0, L, w.n_req, T, case.cu, codes_h,
+                            scales_h, stream)
+        torch.cuda.synchronize(device)
+        staging = torch.empty(B.encoded_staging_bytes(T, s.d_model, chunk, args.e2e_slots),
+                              dtype=torch.uint8, device=device)
+        h2d = codes_h.numel() + scales_h.numel() * 4 + sum(
+            m.numel() * m.element_size() for m in meta_host)
+        enc = (params, codes_h, scales_h)
     t0 = time.perf_counter()
     step_s = []
     for i in range(2 + e2e_steps if e2e_steps > 0 else 0):
@@ -355,7 +370,12 @@ def gpu_arm(args, rank, world, local_rank):
         ts = time.perf_counter()
         for hm, dm in zip(meta_host, meta_dev):
             dm.copy_(hm, non_blocking=True)
-        if split_plan is not None:
+        if enc is not None:
+            B.hcr_restore_streamed_encoded(r.handle, enc[0], enc[1], enc[2], 0, L, w.n_req, T,
+                                           case.cu, case.start, case.table, lay.max_blocks,
+                                           case.k_cache, case.v_cache, layout, staging,
+                                           staging.numel(), chunk, ws, ws.numel(), stream)
+        elif split_plan is not None:
             B.hcr_restore_streamed_split(r.handle, hid_host_split, kv_host, 0,
                                          split_plan["hidden_layers"], L, w.n_req, T, case.cu,
                                          case.start, case.table, lay.max_blocks, case.k_cache,
@@ -488,19 +508,109 @@ def save_arm(args):
     print(json.dumps(line))
 
 
+def codec_arm(args):
+    """Hidden-state codec: encode (device -> device and -> pinned host) and
+    decode (device -> device) of every layer's inputs, HBM-bound kernels."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__._build_module().build()
+    from kv_cache_restoration_gb300 import Restorer, make_dims
+    from kv_cache_restoration_gb300 import binding as B
+    from workloads import configs as C
+    from workloads import generate as G
+
+    device = torch.device("cuda", 0)
+    w = C.get(args.workload)
+    if args.layers:
+        w = C.with_layers(w, args.layers)
+    s = w.shape
+    L, T, d = s.n_layers, w.n_tokens, s.d_model
+    case = G.device_inputs(w, device, gen_device=device)
+    r = Restorer(make_dims(L, d, s.n_heads, s.n_kv_heads, s.head_dim, s.norm, s.norm_eps,
+                           s.rope, s.rope_theta, w.rope_positions, s.dtype, s.kv_bias),
+                 case.params)
+    case.params = None
+    stream = torch.cuda.current_stream(device)
+    peaks, peak_kind = load_peaks()
+    params = B.codec_params()
+    codes = torch.empty((L, T, d), dtype=torch.int8, device=device)
+    scales = torch.zeros((L, T), dtype=torch.float32, device=device)
+    codes_h = torch.empty((L, T, d), dtype=torch.int8).pin_memory()
+    scales_h = torch.zeros((L, T), dtype=torch.float32).pin_memory()
+    out = torch.empty_like(case.hidden)
+
+    def timed(fn, steps, warmup):
+        for _ in range(warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        if r.check(stream)[0] != 0:
+            raise RuntimeError("codec reported a device error")
+        return e0.elapsed_time(e1) / 1e3 / steps
+
+    def enc(cd, sc):
+        return lambda: B.hcr_encode_hidden(r.handle, params, case.hidden, 0, L, w.n_req, T,
+                                           case.cu, cd, sc, stream)
+
+    def dec():
+        B.hcr_decode_hidden(r.handle, params, codes, scales, 0, L, w.n_req, T, case.cu, out,
+                            stream)
+
+    t_enc = timed(enc(codes, scales), args.steps, args.warmup)
+    t_dec = timed(dec, args.steps, args.warmup)
+    t_enc_h = timed(enc(codes_h, scales_h), max(3, args.steps // 10), 2)
+    # algorithmic bytes: bf16 rows in + int8 codes out (encode), the reverse for
+    # decode; scales (one float per 10 rows) are below 1% and not counted
+    moved = 3.0 * L * T * d
+    err = (out.float() - case.hidden.float()).abs()
+    third = [min(2, 3 * l // L) for l in range(L)]
+    err_by_group = [float(err[[l for l in range(L) if third[l] == g]].max())
+                    if g in third else None for g in range(3)]
+    rel_rms = float((err.pow(2).mean() / case.hidden.float().pow(2).mean()).sqrt())
+    line = {
+        "op": "codec",
+        "metric": "encoded tokens/s (all layers' inputs, anchor + delta codec)",
+        "value": T / t_enc, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_enc * 1e3, "higher_is_better": True,
+        "dtype": s.dtype, "data": "synthetic",
+        "config": {"workload": f"{w.name}: {L} layers x {T} tokens x d={d}, groups of 10, "
+                               "bins 0.5/1/1.5"},
+        "roofline": {"bound": "hbm", "achieved": moved / t_enc / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": moved / t_enc / 1e9 / peaks["hbm_gbs"],
+                     "peak_source": f"{peak_kind} HBM copy bandwidth", "kernel": "encode_kernel"},
+        "decode": {"ms_per_step": t_dec * 1e3, "achieved_gbs": moved / t_dec / 1e9,
+                   "frac": moved / t_dec / 1e9 / peaks["hbm_gbs"], "kernel": "decode_kernel"},
+        "encode_to_host": {"ms_per_step": t_enc_h * 1e3,
+                           "write_gbs": L * T * d / t_enc_h / 1e9},
+        "compression": (L * T * d * 2) / (L * T * d + L * -(-T // 10) * 4),
+        "synthetic_error": {"max_abs_by_layer_third": err_by_group, "relative_rms": rel_rms,
+                            "note": "N(0,1) synthetic hidden states; no quality claim"},
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--op", default="restore", choices=["restore", "save"],
+    ap.add_argument("--op", default="restore", choices=["restore", "save", "codec"],
                     help="restore (the benchmark step) or save (hcr_save_hidden)")
     ap.add_argument("--workload", default="llama2-7b")
     ap.add_argument("--e2e-steps", type=int, default=30, help="0 skips the end-to-end leg")
     ap.add_argument("--e2e-chunk", type=int, default=4, help="layers per streamed chunk")
     ap.add_argument("--e2e-slots", type=int, default=3, help="staging ring slots")
-    ap.add_argument("--e2e-source", default="layers", choices=["layers", "chunks", "split"],
+    ap.add_argument("--e2e-source", default="layers",
+                    choices=["layers", "chunks", "split", "encoded"],
                     help="host form of the saved state: [layer][token][d] hidden states, the "
                          "saved chunk store, or the planned split of hidden states and K/V")
     ap.add_argument("--split-layer", type=int, default=-1,
@@ -525,6 +635,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.op == "save":
         return save_arm(args)
+    if args.op == "codec":
+        return codec_arm(args)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -637,7 +749,9 @@ def main():
                                    f"{args.e2e_chunk_tokens}-token chunks, {res['chunk']}-layer "
                                    "groups, ",
                          "split": f"hcr_restore_streamed_split (hidden states below the split, "
-                                  f"saved K/V above), {res['chunk']}-layer groups, "}[
+                                  f"saved K/V above), {res['chunk']}-layer groups, ",
+                         "encoded": f"hcr_restore_streamed_encoded (int8 anchor + delta codes, "
+                                    f"decoded on the GPU), {res['chunk']}-layer groups, "}[
                             args.e2e_source] + f"{args.e2e_slots}-slot staging ring",
                  "layer_split": res["split"],
                  "plain_h2d_gbs": res["h2d_gbs"]}

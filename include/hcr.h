@@ -403,10 +403,11 @@ hcr_status hcr_restore_streamed_split(hcr_handle* h, const void* hidden_host,
  *
  *   groups:  token i of a request belongs to the group whose anchor is token
  *            group_tokens * (i / group_tokens) of the same request;
- *   anchor:  s = max|h| / 127 (float32), q = rint(h / s) in [-127, 127]
- *            (all 0 when s = 0); decoded q * s;
- *   others:  c = rint((h - q s) / b) in [-127, 127]; decoded q s + c b, with
- *            b = bins[min(2, 3 l / n_layers)] for model layer l;
+ *   anchor:  s = max|h| / 127 (float32), q = rint(h * (1 / s)) in
+ *            [-127, 127]; s = 0 and all codes 0 when s < 2^-126; decoded q * s;
+ *   others:  c = rint((h - q s) * (1 / b)) in [-127, 127]; decoded q s + c b,
+ *            with b = bins[min(2, 3 l / n_layers)] for model layer l;
+ *   1 / s and 1 / b are single binary32 divisions;
  *   every step one IEEE binary32 operation rounded to nearest even; the
  *   decoded value rounded once to the storage dtype.
  *

@@ -13,9 +13,12 @@
 // This library's reading, fixed here and in the oracle alike:
 //   * groups are formed per request (token i of a request belongs to the group
 //     whose anchor is token G * (i / G) of that request);
-//   * anchor row: scale s = max|h| / 127, code q = rint(h / s) in [-127, 127];
-//   * other rows: code c = rint((h - q s) / b) in [-127, 127] -- the delta from
-//     the anchor as the decoder sees it; decoded value q s + c b;
+//   * anchor row: scale s = max|h| / 127, code q = rint(h * (1 / s)) in
+//     [-127, 127]; a row with s below 2^-126 codes as all zero (s = 0);
+//   * other rows: code c = rint((h - q s) * (1 / b)) in [-127, 127] -- the
+//     delta from the anchor as the decoder sees it; decoded value q s + c b;
+//   * the reciprocals 1 / s (per anchor row) and 1 / b (per layer) are one
+//     binary32 division each, so the per-element work is multiplications;
 //   * layer l of L uses bin bins[min(2, 3 l / L)];
 //   * every step is one IEEE binary32 operation rounded to nearest even (the
 //     _rn intrinsics keep the compiler from contracting them), so the codes
@@ -24,10 +27,12 @@
 // Encoded form: codes int8 [layer][token][d_model] and scales float32
 // [layer][token] (entries of non-anchor rows are left untouched).
 //
-// encode_kernel: one warp per anchor (warps of other rows exit at once);
-// grid.y runs over layers.  The warp reduces the anchor's max|h|, then
-// streams the group's rows in 16-byte vectors (8 elements per lane), the
-// decoded anchor recomputed per vector.  decode_kernel: one warp per token
+// encode_kernel: four warps per group (groups numbered request by request; a
+// warp finds its group by a scan over the requests); grid.y runs over layers.
+// Each warp reduces the anchor's max|h| over the whole row, then streams its
+// quarter of the 16-byte vectors (8 elements per lane) of every row of the
+// group, the decoded anchor recomputed per vector and four rows loaded before
+// their codes are stored.  decode_kernel: one warp per token
 // row, grid.y over layers; a row reads its anchor's codes and scale and its
 // own codes and writes the storage type.  Both are HBM-bound; a row with no
 // request (cu_seqlens inconsistent with n_tokens) is skipped and flagged.
@@ -42,6 +47,8 @@ namespace hcr {
 namespace {
 
 constexpr int kCodecThreads = 256;
+constexpr int kWarpsPerGroup = 4;   // encode: warps sharing one group's rows (the max is
+                                    // reduced by each over the whole anchor row)
 
 struct CodecParams {
   const uint16_t* hidden;   // encode: input [Lr][T][d]
@@ -122,53 +129,88 @@ __device__ __forceinline__ float layer_bin(const CodecParams& p, int li) {
   return g == 0 ? p.bins[0] : (g == 1 ? p.bins[1] : p.bins[2]);   // no indexed param array
 }
 
+// Group k of a layer (groups numbered request by request): its anchor token
+// and row count, or n = 0 past the last group.  A linear scan over the
+// requests; rows past n_tokens are never addressed (flagged instead).
+__device__ __forceinline__ void group_of(const CodecParams& p, int k, int* t, int* n) {
+  int base = 0;
+  *n = 0;
+  for (int r = 0; r < p.n_req; ++r) {
+    const int c0 = __ldg(p.cu_seqlens + r), c1 = __ldg(p.cu_seqlens + r + 1);
+    const int len = max(0, c1 - c0);
+    const int g = (len + p.group_tokens - 1) / p.group_tokens;
+    if (k < base + g) {
+      *t = c0 + (k - base) * p.group_tokens;
+      *n = min(p.group_tokens, c1 - *t);
+      if (*t < 0 || *t + *n > p.n_tokens) {
+        atomicOr(p.err, uint32_t(HCR_DEVERR_SEQLENS));
+        *n = 0;
+      }
+      return;
+    }
+    base += g;
+  }
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kCodecThreads) encode_kernel(const CodecParams p) {
+  constexpr int kBatch = 4;   // group rows loaded together before their codes are stored
   const int lane = threadIdx.x & 31;
   const int li = blockIdx.y;
-  const int warp0 = int((blockIdx.x * kCodecThreads + threadIdx.x) >> 5);
-  const int nwarps = int((gridDim.x * kCodecThreads) >> 5);
+  const int wid = int((blockIdx.x * kCodecThreads + threadIdx.x) >> 5);
+  const int k = wid / kWarpsPerGroup;       // the group
+  const int part = wid % kWarpsPerGroup;    // this warp's share of each row's vectors
   const int nvec = p.d_model >> 3;
   const float b = layer_bin(p, li);
-  for (int t = warp0; t < p.n_tokens; t += nwarps) {
-    int c0, c1;
-    if (request_of(p, t, &c0, &c1) < 0) {
-      if (lane == 0) atomicOr(p.err, uint32_t(HCR_DEVERR_SEQLENS));
-      continue;
+  if (wid == 0 && li == 0 && lane == 0 &&
+      (__ldg(p.cu_seqlens) != 0 || __ldg(p.cu_seqlens + p.n_req) != p.n_tokens))
+    atomicOr(p.err, uint32_t(HCR_DEVERR_SEQLENS));
+  int t = 0, n = 0;
+  group_of(p, k, &t, &n);
+  if (n == 0) return;
+  const int64_t row0 = int64_t(li) * p.n_tokens + t;
+  const uint4* __restrict__ src = reinterpret_cast<const uint4*>(p.hidden + row0 * p.d_model);
+  uint2* __restrict__ dst = reinterpret_cast<uint2*>(p.codes + row0 * p.d_model);
+  float m = 0.f;
+#pragma unroll 4
+  for (int v = lane; v < nvec; v += 32) {
+    float x[8];
+    widen8<DT>(__ldg(src + v), x);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  // a row below 127 * 2^-126 codes as all zero, so 1 / s stays finite
+  const float s_raw = __fdiv_rn(m, 127.f);
+  const float s = s_raw < 1.17549435e-38f ? 0.f : s_raw;
+  const float inv_s = s == 0.f ? 0.f : __fdiv_rn(1.f, s);
+  const float inv_b = __fdiv_rn(1.f, b);
+  if (lane == 0 && part == 0) p.scales[row0] = s;
+  for (int v = part * 32 + lane; v < nvec; v += 32 * kWarpsPerGroup) {
+    float x[8], a_hat[8];
+    int8_t q[8];
+    widen8<DT>(__ldg(src + v), x);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      q[i] = s == 0.f ? int8_t(0) : code_of(__fmul_rn(x[i], inv_s));
+      a_hat[i] = __fmul_rn(float(q[i]), s);
     }
-    if ((t - c0) % p.group_tokens != 0) continue;   // not an anchor
-    const int n = min(p.group_tokens, c1 - t);
-    const int64_t row0 = int64_t(li) * p.n_tokens + t;
-    const uint4* a_vec = reinterpret_cast<const uint4*>(p.hidden + row0 * p.d_model);
-    float m = 0.f;
-    for (int v = lane; v < nvec; v += 32) {
-      float x[8];
-      widen8<DT>(__ldg(a_vec + v), x);
+    dst[v] = pack_codes(q);
+    for (int j0 = 1; j0 < n; j0 += kBatch) {
+      uint4 raw[kBatch];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(x[k]));
-    }
+      for (int u = 0; u < kBatch; ++u)
+        if (j0 + u < n) raw[u] = __ldg(src + int64_t(j0 + u) * nvec + v);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float s = __fdiv_rn(m, 127.f);
-    if (lane == 0) p.scales[row0] = s;
-    for (int v = lane; v < nvec; v += 32) {
-      float x[8], a_hat[8];
-      int8_t q[8];
-      widen8<DT>(__ldg(a_vec + v), x);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        q[k] = s == 0.f ? int8_t(0) : code_of(__fdiv_rn(x[k], s));
-        a_hat[k] = __fmul_rn(float(q[k]), s);
-      }
-      reinterpret_cast<uint2*>(p.codes + row0 * p.d_model)[v] = pack_codes(q);
-      for (int j = 1; j < n; ++j) {
-        const int64_t row = row0 + j;
+      for (int u = 0; u < kBatch; ++u) {
+        if (j0 + u >= n) break;
         float y[8];
         int8_t c[8];
-        widen8<DT>(__ldg(reinterpret_cast<const uint4*>(p.hidden + row * p.d_model) + v), y);
+        widen8<DT>(raw[u], y);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) c[k] = code_of(__fdiv_rn(__fsub_rn(y[k], a_hat[k]), b));
-        reinterpret_cast<uint2*>(p.codes + row * p.d_model)[v] = pack_codes(c);
+        for (int i = 0; i < 8; ++i) c[i] = code_of(__fmul_rn(__fsub_rn(y[i], a_hat[i]), inv_b));
+        dst[int64_t(j0 + u) * nvec + v] = pack_codes(c);
       }
     }
   }
@@ -295,8 +337,13 @@ extern "C" hcr_status hcr_encode_hidden(hcr_handle* h, const hcr_codec_params* c
   p.codes = static_cast<int8_t*>(dcodes);
   p.scales = static_cast<float*>(dscales);
   const int32_t nl = layer_end - layer_begin;
-  // one anchor in group_tokens rows does the work
-  const dim3 grid = codec_grid(h, n_tokens, nl, 1);
+  // one warp per group: at most one group per request plus one per
+  // group_tokens tokens
+  const int64_t groups = int64_t(n_req) + (int64_t(n_tokens) + cp->group_tokens - 1) /
+                                              cp->group_tokens;
+  const int64_t blocks = (groups * kWarpsPerGroup * 32 + kCodecThreads - 1) / kCodecThreads;
+  if (blocks > INT32_MAX) return set_last_error(HCR_ERR_UNSUPPORTED, "too many groups");
+  const dim3 grid{unsigned(blocks), unsigned(nl)};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.dtype == HCR_DTYPE_BF16)
     encode_kernel<HCR_DTYPE_BF16><<<grid, kCodecThreads, 0, s>>>(p);

@@ -23,11 +23,15 @@ Readings (listed in the design notes too):
     whose anchor is token 10 * (i // 10) of the same request; a request's last
     group may be shorter;
   * anchor quantisation is symmetric per row: scale s = max|h| / 127,
-    code q = round(h / s) in [-127, 127], value q * s (all codes 0 when the
-    row is all zero);
+    code q = round(h * (1 / s)) in [-127, 127], value q * s; a row whose s is
+    below the smallest normal binary32 number (max|h| < 127 * 2^-126) is
+    coded as all zero with s = 0, so 1 / s is always finite;
   * a delta is taken from the anchor as the decoder will see it (q * s), so
-    its error is the delta quantisation's alone: code c = round((h - q s) / b)
-    clamped to [-127, 127], value q s + c b;
+    its error is the delta quantisation's alone: code
+    c = round((h - q s) * (1 / b)) clamped to [-127, 127], value q s + c b;
+  * quantising multiplies by the reciprocal of the step (1 / s once per
+    anchor row, 1 / b once per layer), each reciprocal one binary32 division:
+    the page gives the step sizes, not the arithmetic;
   * a bin b is in the hidden states' own units; layer l of L uses bin
     bins[min(2, 3 l // L)];
   * all arithmetic is IEEE binary32 with round-half-to-even for round(), the
@@ -72,14 +76,18 @@ def rint32(x: np.ndarray) -> np.ndarray:
     return np.rint(np.asarray(x, F32)).astype(F32)
 
 
+SMALLEST_NORMAL = F32(np.finfo(F32).tiny)   # 2^-126
+
+
 def quantise_anchor(h: np.ndarray) -> Tuple[np.ndarray, np.float32]:
     """8-bit symmetric quantisation of one float32 row: (codes int8, scale)."""
     h = np.asarray(h, F32)
     m = F32(np.max(np.abs(h))) if h.size else F32(0)
     s = F32(m / F32(127))
-    if s == 0:
+    if s < SMALLEST_NORMAL:
         return np.zeros(h.shape, np.int8), F32(0)
-    q = np.clip(rint32(h / s), -127, 127)
+    inv = F32(F32(1) / s)
+    q = np.clip(rint32((h * inv).astype(F32)), -127, 127)
     return q.astype(np.int8), s
 
 
@@ -102,7 +110,8 @@ def encode_layer(h: np.ndarray, anchors: np.ndarray, b: np.float32):
             continue
         a_hat = dequantise_anchor(codes[a], scales[a])
         delta = (h[t] - a_hat).astype(F32)
-        codes[t] = np.clip(rint32(delta / F32(b)), -127, 127).astype(np.int8)
+        inv_b = F32(F32(1) / F32(b))
+        codes[t] = np.clip(rint32((delta * inv_b).astype(F32)), -127, 127).astype(np.int8)
     return codes, scales
 
 

@@ -148,3 +148,30 @@ def test_multi_layer_encode_uses_each_layers_bin():
         assert np.array_equal(codes[i], c) and np.array_equal(scales[i], s)
     dec = K.decode(codes, scales, 0, 3, cu)
     assert dec.shape == (3, 12, 8)
+
+
+def test_tiny_rows_code_as_zero():
+    """max|h| below 127 * 2^-126: scale 0 and all codes 0, so 1 / s stays finite."""
+    h = np.zeros((2, 4), F32)
+    h[0] = [1e-37, -2e-37, 0.0, 5e-38]
+    h[1] = [1.0, 0.0, 0.0, 0.0]
+    anchors = K.group_anchors([0, 2])
+    codes, scales = K.encode_layer(h, anchors, F32(0.5))
+    assert scales[0] == 0 and (codes[0] == 0).all()
+    assert codes[1].tolist() == [2, 0, 0, 0]
+    q, s = K.quantise_anchor(np.array([127 * 2.0 ** -126, 0.0], F32))
+    assert s == F32(2.0 ** -126) and q.tolist() == [127, 0]
+
+
+def test_reciprocal_step_differs_from_division_only_by_rounding():
+    """The codes use x * (1/b); against x / b they differ by at most one step,
+    and only where x / b sits within a rounding of a half-integer."""
+    rng = np.random.default_rng(2)
+    x = (rng.standard_normal(200000) * 50).astype(F32)
+    for b in (0.5, 1.0, 1.5, 0.3):
+        inv = F32(F32(1) / F32(b))
+        a = K.rint32((x * inv).astype(F32))
+        d = K.rint32((x / F32(b)).astype(F32))
+        assert np.abs(a - d).max() <= 1
+        if b in (0.5, 1.0):           # power-of-two steps: identical
+            assert np.array_equal(a, d)

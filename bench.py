@@ -409,12 +409,14 @@ def gpu_arm(args, rank, world, local_rank):
 
     t_step = total_ms / 1e3 / args.steps
     e2e_med = statistics.median(step_s) if step_s else float("nan")
-    t_step, proj_ms, prep_ms, e2e_s, e2e_med = reduce_max_over_ranks(
-        [t_step, proj_ms, prep_ms, e2e_s, e2e_med], device)
+    e2e_p90 = sorted(step_s)[int(0.9 * (len(step_s) - 1))] if step_s else float("nan")
+    e2e_max = max(step_s) if step_s else float("nan")
+    t_step, proj_ms, prep_ms, e2e_s, e2e_med, e2e_p90, e2e_max = reduce_max_over_ranks(
+        [t_step, proj_ms, prep_ms, e2e_s, e2e_med, e2e_p90, e2e_max], device)
     return dict(w=w, t_step=t_step, proj_ms=proj_ms, prep_ms=prep_ms, e2e_s=e2e_s, h2d=h2d,
                 clocks=clk.summary(), launches=2 * args.steps, h2d_gbs=h2d_gbs, chunk=chunk,
                 split=split_plan,
-                e2e_median_s=e2e_med)
+                e2e_median_s=e2e_med, e2e_p90_s=e2e_p90, e2e_max_s=e2e_max)
 
 
 def save_arm(args):
@@ -744,6 +746,8 @@ def main():
                  "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": 4,
                  "ms_per_step": res["e2e_s"] * 1e3,
                  "ms_per_step_median": res["e2e_median_s"] * 1e3,
+                 "ms_per_step_p90": res["e2e_p90_s"] * 1e3,
+                 "ms_per_step_max": res["e2e_max_s"] * 1e3,
                  "api": {"layers": f"hcr_restore_streamed, {res['chunk']}-layer chunks, ",
                          "chunks": f"hcr_restore_streamed_chunks from a pinned host store of "
                                    f"{args.e2e_chunk_tokens}-token chunks, {res['chunk']}-layer "

@@ -22,7 +22,7 @@ LIB = os.path.join(PKG, "libhcr.so")
 SOURCES = ["hcr_api.cu", "hcr_prepare.cu", "hcr_project.cu", "hcr_no_alloc.cu",
            "hcr_streamed.cu", "hcr_save.cu", "hcr_kv.cu", "hcr_plan.cu",
            "hcr_codec.cu"]
-HEADERS = ["hcr_internal.h", "ptx.cuh"]
+HEADERS = ["hcr_internal.h", "hcr_host.h", "ptx.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -10,7 +10,7 @@
 #include <string>
 #include <vector>
 
-#include "hcr_internal.h"
+#include "hcr_host.h"
 
 namespace hcr {
 namespace {

@@ -41,7 +41,7 @@
 
 #include <cmath>
 
-#include "hcr_internal.h"
+#include "hcr_host.h"
 
 namespace hcr {
 namespace {

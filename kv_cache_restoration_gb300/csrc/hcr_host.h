@@ -1,0 +1,73 @@
+// Host-side declarations shared by the library's entry points: the handle,
+// error recording, NVTX ranges, and launchers of the kernels outside the
+// restore itself.  Not part of the public ABI.
+#pragma once
+
+#include <nvtx3/nvToolsExt.h>
+
+#include "hcr_internal.h"
+
+namespace hcr {
+
+constexpr int kMaxStagingSlots = 8;    // staging ring of the layer-pipelined restore
+
+struct StreamedRes;  // copy stream + events of hcr_restore_streamed (hcr_streamed.cu)
+
+// ---------------------------------------------------------------------------
+// Handle
+// ---------------------------------------------------------------------------
+struct Handle {
+  hcr_model_dims dims;
+  int device = 0;
+  int num_sms = 0;
+  void* w_packed = nullptr;    // [L][2*d_kv][d] storage dtype, gamma folded in
+  float* col_sum = nullptr;    // [L][2*d_kv] sum_i W'[j][i] (LayerNorm only)
+  float* col_bias = nullptr;   // [L][2*d_kv] folded bias (LN: W beta + b; RMS: b), or null
+  float2* rope_tab = nullptr;  // [max_position][head_dim/2] (cos, sin), or null
+  uint32_t* err = nullptr;     // device error word (HCR_DEVERR_* bits)
+  CUtensorMap tmap_w;          // 3-D map over w_packed: (d, 2*d_kv, L), box (64, 256, 1)
+  CUtensorMap tmap_w_half;     // same tensor, box (64, 128, 1): half a tile per CTA of a pair
+  int pair_clusters = 0;       // co-resident CTA pairs of the pair variant (0: unavailable)
+  uint32_t debug_stall = 0;    // test hook: see hcr_debug_set_stall
+  int32_t variant = 0;         // test hook: 0 auto, 1 single CTAs, 2 CTA pairs
+  StreamedRes* streamed = nullptr;  // created on the first hcr_restore_streamed call
+};
+
+void release_streamed(Handle& H);
+
+// Records a message for hcr_last_error() on this host thread; returns s.
+hcr_status set_last_error(hcr_status s, const char* fmt, ...);
+
+// An NVTX range on the calling host thread for the scope's lifetime: the
+// library's entry points and stages show up by name in a timeline profiler
+// (nothing is recorded when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+// Rows of K and V between the paged cache and a dense [layer][K|V][token][row]
+// store (hcr_kv.cu).  Pointers to host memory are the device's mapped view.
+struct KvRowsParams {
+  const int64_t* slot;     // [T] from the prepare kernel; -1 rows are skipped
+  uint4* dense;            // [n_layers][2][T][row_vecs]
+  void* k_cache;           // base of the first layer
+  void* v_cache;
+  int64_t layer_stride_vecs;
+  int32_t row_vecs;        // n_kv_heads * head_dim / 8
+  int32_t n_tokens, n_layers;
+};
+
+cudaError_t launch_kv_rows(const KvRowsParams& p, bool to_cache, int num_sms, cudaStream_t s);
+// The device address of caller memory that may live on the host (mapped pinned
+// memory, or pageable memory when the device can reach it); an error status
+// names `what` when the device cannot address it.
+hcr_status device_view(const Handle& H, void* ptr, const char* what, void** out);
+
+}  // namespace hcr
+
+struct hcr_handle {
+  hcr::Handle impl;
+};

@@ -1,5 +1,7 @@
-// Internal declarations shared by the host API (hcr_api.cu) and the kernels
-// (hcr_prepare.cu, hcr_project.cu).  Not part of the public ABI.
+// Internal declarations the restore kernels (hcr_prepare.cu, hcr_project.cu)
+// are compiled from: tiling constants, the instruction descriptor, the
+// workspace layout, kernel parameters and their launchers.  Host-only
+// declarations live in hcr_host.h.  Not part of the public ABI.
 #pragma once
 
 #include <cuda.h>
@@ -7,8 +9,6 @@
 
 #include <cstddef>
 #include <cstdint>
-
-#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/hcr.h"
 
@@ -56,32 +56,6 @@ constexpr uint32_t make_idesc_f16(int dtype, int m, int n) {
          (uint32_t(dtype == HCR_DTYPE_BF16 ? 1 : 0) << 10) | (uint32_t(n >> 3) << 17) |
          (uint32_t(m >> 4) << 24);
 }
-
-constexpr int kMaxStagingSlots = 8;    // staging ring of the layer-pipelined restore
-
-struct StreamedRes;  // copy stream + events of hcr_restore_streamed (hcr_streamed.cu)
-
-// ---------------------------------------------------------------------------
-// Handle
-// ---------------------------------------------------------------------------
-struct Handle {
-  hcr_model_dims dims;
-  int device = 0;
-  int num_sms = 0;
-  void* w_packed = nullptr;    // [L][2*d_kv][d] storage dtype, gamma folded in
-  float* col_sum = nullptr;    // [L][2*d_kv] sum_i W'[j][i] (LayerNorm only)
-  float* col_bias = nullptr;   // [L][2*d_kv] folded bias (LN: W beta + b; RMS: b), or null
-  float2* rope_tab = nullptr;  // [max_position][head_dim/2] (cos, sin), or null
-  uint32_t* err = nullptr;     // device error word (HCR_DEVERR_* bits)
-  CUtensorMap tmap_w;          // 3-D map over w_packed: (d, 2*d_kv, L), box (64, 256, 1)
-  CUtensorMap tmap_w_half;     // same tensor, box (64, 128, 1): half a tile per CTA of a pair
-  int pair_clusters = 0;       // co-resident CTA pairs of the pair variant (0: unavailable)
-  uint32_t debug_stall = 0;    // test hook: see hcr_debug_set_stall
-  int32_t variant = 0;         // test hook: 0 auto, 1 single CTAs, 2 CTA pairs
-  StreamedRes* streamed = nullptr;  // created on the first hcr_restore_streamed call
-};
-
-void release_streamed(Handle& H);
 
 // ---------------------------------------------------------------------------
 // Workspace layout (all offsets 256-byte aligned)
@@ -148,40 +122,10 @@ struct ProjectParams {
   uint32_t debug_stall;
 };
 
-// Rows of K and V between the paged cache and a dense [layer][K|V][token][row]
-// store (hcr_kv.cu).  Pointers to host memory are the device's mapped view.
-struct KvRowsParams {
-  const int64_t* slot;     // [T] from the prepare kernel; -1 rows are skipped
-  uint4* dense;            // [n_layers][2][T][row_vecs]
-  void* k_cache;           // base of the first layer
-  void* v_cache;
-  int64_t layer_stride_vecs;
-  int32_t row_vecs;        // n_kv_heads * head_dim / 8
-  int32_t n_tokens, n_layers;
-};
-
-// An NVTX range on the calling host thread for the scope's lifetime: the
-// library's entry points and stages show up by name in a timeline profiler
-// (nothing is recorded when no tool is attached).
-struct NvtxRange {
-  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
-  ~NvtxRange() { nvtxRangePop(); }
-  NvtxRange(const NvtxRange&) = delete;
-  NvtxRange& operator=(const NvtxRange&) = delete;
-};
-
-// Records a message for hcr_last_error() on this host thread; returns s.
-hcr_status set_last_error(hcr_status s, const char* fmt, ...);
-
 // Launchers (return cudaGetLastError() of the launch).
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t s);
 cudaError_t launch_project(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
                            const ProjectParams& p, int grid, bool pair, cudaStream_t s);
-cudaError_t launch_kv_rows(const KvRowsParams& p, bool to_cache, int num_sms, cudaStream_t s);
-// The device address of caller memory that may live on the host (mapped pinned
-// memory, or pageable memory when the device can reach it); an error status
-// names `what` when the device cannot address it.
-hcr_status device_view(const Handle& H, void* ptr, const char* what, void** out);
 // Co-resident clusters of the CTA-pair variant on the current device (< 0 on error).
 int project_pair_clusters(int dtype);
 cudaError_t launch_pack_weights(const void* w_k, const void* w_v, const void* gamma, void* dst,
@@ -193,6 +137,3 @@ cudaError_t launch_column_constants(const void* w_packed, const void* w_k, const
 
 }  // namespace hcr
 
-struct hcr_handle {
-  hcr::Handle impl;
-};

@@ -13,7 +13,7 @@
 // them).  One warp per row, 16-byte vectors, four in flight per lane; the
 // grid strides over rows.  Either side may be device memory or mapped host
 // memory.
-#include "hcr_internal.h"
+#include "hcr_host.h"
 
 namespace hcr {
 namespace {

@@ -17,7 +17,7 @@
 // kernels like any caller-provided workspace.
 #include <mutex>
 
-#include "hcr_internal.h"
+#include "hcr_host.h"
 
 namespace hcr {
 namespace {

@@ -32,7 +32,7 @@
 #include <cstring>
 #include <vector>
 
-#include "hcr_internal.h"
+#include "hcr_host.h"
 
 namespace hcr {
 namespace {

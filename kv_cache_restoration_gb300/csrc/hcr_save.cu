@@ -18,7 +18,7 @@
 // handle's device error word.  The chunk store may be device memory or
 // pinned host memory the device can address: then these stores cross the
 // host link directly and no separate snapshot copy is needed.
-#include "hcr_internal.h"
+#include "hcr_host.h"
 
 namespace hcr {
 namespace {

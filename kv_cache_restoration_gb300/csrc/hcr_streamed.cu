@@ -23,7 +23,7 @@
 #include <mutex>
 #include <vector>
 
-#include "hcr_internal.h"
+#include "hcr_host.h"
 
 namespace hcr {
 

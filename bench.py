@@ -230,7 +230,14 @@ def gpu_arm(args, rank, world, local_rank):
     if args.layers:
         w = C.with_layers(w, args.layers)
     s = w.shape
-    case = G.device_inputs(w, device, gen_device=device)
+    # A workload whose hidden states and caches for all layers exceed HBM (the
+    # ragged batch) restores in windows of layers: one window of buffers is
+    # allocated and every window's restore reads it, back to back, so the step
+    # is the whole restore at the GPU's sustained load.
+    win = args.window_layers if args.window_layers >= 0 else (8 if w.name == "ragged-7b" else 0)
+    win = min(win, s.n_layers) if win > 0 else s.n_layers
+    windows = [(lb, min(lb + win, s.n_layers)) for lb in range(0, s.n_layers, win)]
+    case = G.device_inputs(w, device, 0, win, gen_device=device)
     r = Restorer(make_dims(s.n_layers, s.d_model, s.n_heads, s.n_kv_heads, s.head_dim, s.norm,
                            s.norm_eps, s.rope, s.rope_theta, w.rope_positions, s.dtype,
                            s.kv_bias), case.params)
@@ -241,22 +248,26 @@ def gpu_arm(args, rank, world, local_rank):
             raise RuntimeError(B.hcr_last_error())
     lay = case.layout
     L, T = s.n_layers, w.n_tokens
-    ws = r.workspace(T, L, device)
+    ws = r.workspace(T, win, device)
     stream = torch.cuda.current_stream(device)
 
-    def stage(name):
-        r.restore(case.hidden, 0, L, case.cu, case.start, case.table, case.k_cache,
+    def stage(name, lb=0, le=None):
+        le = L if le is None else le
+        r.restore(case.hidden[:le - lb], lb, le, case.cu, case.start, case.table, case.k_cache,
                   case.v_cache, lay.num_blocks, lay.block_size, stream=stream, workspace=ws,
                   stage=name)
 
     for _ in range(args.warmup):
-        stage("prepare")
-        stage("project")
+        for lb, le in windows:
+            stage("prepare", lb, le)
+            stage("project", lb, le)
     st, flags = r.check(stream)
     if st != 0:
         raise RuntimeError(f"restore reported device error {st} flags {flags:#x}")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    nw = len(windows)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nw + 1)]
+          for _ in range(args.steps)]
     gpu_id = getattr(torch.cuda.get_device_properties(device), "uuid", None)
     gpu_id = f"GPU-{gpu_id}" if gpu_id is not None else str(local_rank)
     torch.cuda.synchronize(device)
@@ -266,16 +277,19 @@ def gpu_arm(args, rank, world, local_rank):
         torch.cuda.synchronize(device)
         for i in range(args.steps):
             ev[i][0].record(stream)
-            stage("prepare")
-            ev[i][1].record(stream)
-            stage("project")
-            ev[i][2].record(stream)
+            for k, (lb, le) in enumerate(windows):
+                stage("prepare", lb, le)
+                ev[i][2 * k + 1].record(stream)
+                stage("project", lb, le)
+                ev[i][2 * k + 2].record(stream)
         torch.cuda.synchronize(device)
     if world > 1:
         dist.barrier()
-    total_ms = ev[0][0].elapsed_time(ev[-1][2])
-    prep_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    proj_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    total_ms = ev[0][0].elapsed_time(ev[-1][-1])
+    prep_ms = statistics.mean(sum(e[2 * k].elapsed_time(e[2 * k + 1]) for k in range(nw))
+                              for e in ev)
+    proj_ms = statistics.mean(sum(e[2 * k + 1].elapsed_time(e[2 * k + 2]) for k in range(nw))
+                              for e in ev)
     st, flags = r.check(stream)
     if st != 0:
         raise RuntimeError(f"restore reported device error {st} flags {flags:#x}")
@@ -293,7 +307,9 @@ def gpu_arm(args, rank, world, local_rank):
     chunk_bytes = chunk * T * s.d_model * 2
     staging = torch.empty(args.e2e_slots * chunk_bytes, dtype=torch.uint8, device=device)
     layout = B.hcr_cache_layout(lay.num_blocks, lay.block_size, 0)
-    e2e_steps = min(args.steps, args.e2e_steps)
+    # the end-to-end leg needs every layer's hidden states in host memory and
+    # one restore over them; a windowed workload has no such leg
+    e2e_steps = min(args.steps, args.e2e_steps) if nw == 1 else 0
     src = None
     if args.e2e_source == "chunks" and e2e_steps > 0:
         # The saved form: 64-token chunks [chunk][layer][row][d] in pinned host
@@ -414,7 +430,8 @@ def gpu_arm(args, rank, world, local_rank):
     t_step, proj_ms, prep_ms, e2e_s, e2e_med, e2e_p90, e2e_max = reduce_max_over_ranks(
         [t_step, proj_ms, prep_ms, e2e_s, e2e_med, e2e_p90, e2e_max], device)
     return dict(w=w, t_step=t_step, proj_ms=proj_ms, prep_ms=prep_ms, e2e_s=e2e_s, h2d=h2d,
-                clocks=clk.summary(), launches=2 * args.steps, h2d_gbs=h2d_gbs, chunk=chunk,
+                clocks=clk.summary(), launches=2 * nw * args.steps, windows=windows,
+                h2d_gbs=h2d_gbs, chunk=chunk,
                 split=split_plan,
                 e2e_median_s=e2e_med, e2e_p90_s=e2e_p90, e2e_max_s=e2e_max)
 
@@ -618,6 +635,9 @@ def main():
     ap.add_argument("--split-layer", type=int, default=-1,
                     help="with --e2e-source split: first K/V layer (default: the planner's)")
     ap.add_argument("--e2e-chunk-tokens", type=int, default=64, help="tokens per saved chunk")
+    ap.add_argument("--window-layers", type=int, default=-1,
+                    help="restore in windows of this many layers (0: all at once; default: 8 "
+                         "for the ragged batch, whose buffers exceed HBM, else all at once)")
     ap.add_argument("--variant", type=int, default=0,
                     help="project kernel tiles: 0 automatic, 1 single CTAs, 2 CTA pairs")
     ap.add_argument("--layers", type=int, default=0,
@@ -735,7 +755,14 @@ def main():
                    "project_variant": {0: "auto", 1: "single", 2: "pair"}[args.variant],
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2 ({(hid_b + w_b + kv_b) / 1e9:.2f} GB "
-                         "moved per step vs 129 MB L2); no flush"},
+                         "moved per step vs 129 MB L2); no flush",
+                   **({"layer_windows": f"{len(res['windows'])} windows of "
+                                        f"{res['windows'][0][1] - res['windows'][0][0]} layers "
+                                        "restored back to back per step; hidden states and "
+                                        "caches of all layers exceed HBM, so one window of "
+                                        "buffers is allocated and every window reads and "
+                                        "writes it"}
+                      if len(res["windows"]) > 1 else {})},
         "kv_gbs": kv_gbs,
         "step_roofline_frac": roof_t / t,
         "stage_ms": {"prepare": res["prep_ms"], "project": res["proj_ms"]},

@@ -125,7 +125,7 @@ struct RestoreArgs {
 // whether the workspace must hold norm statistics for the layer range, not
 // only the slot map.
 hcr_status validate_restore(const hcr_handle* h, const RestoreArgs& a, bool* empty,
-                            bool stats = true) {
+                            bool stats = true, const char* input = "hidden") {
   *empty = false;
   if (!h) return fail(HCR_ERR_INVALID_ARG, "handle is NULL");
   const hcr_model_dims& d = h->impl.dims;
@@ -139,8 +139,9 @@ hcr_status validate_restore(const hcr_handle* h, const RestoreArgs& a, bool* emp
     return HCR_OK;
   }
   if (a.n_req < 1) return fail(HCR_ERR_INVALID_ARG, "n_tokens > 0 needs n_req >= 1");
-  if (!a.hidden) return fail(HCR_ERR_INVALID_ARG, "hidden is NULL");
-  if (!aligned(a.hidden, 16)) return fail(HCR_ERR_INVALID_ARG, "hidden must be 16-byte aligned");
+  if (!a.hidden) return fail(HCR_ERR_INVALID_ARG, "%s is NULL", input);
+  if (!aligned(a.hidden, 16))
+    return fail(HCR_ERR_INVALID_ARG, "%s must be 16-byte aligned", input);
   if (!a.cu_seqlens || !a.start_pos || !a.block_table)
     return fail(HCR_ERR_INVALID_ARG, "cu_seqlens, start_pos and block_table must be non-NULL");
   if (a.max_blocks < 1) return fail(HCR_ERR_INVALID_ARG, "max_blocks_per_req must be >= 1");
@@ -501,7 +502,7 @@ hcr_status hcr_restore(hcr_handle* h, const void* hidden, int32_t layer_begin, i
 static hcr_status kv_rows(hcr_handle* h, const RestoreArgs& a, bool to_cache, const char* what) {
   NvtxRange range(to_cache ? "hcr_load_kv" : "hcr_save_kv");
   bool empty = false;
-  hcr_status st = validate_restore(h, a, &empty, /*stats=*/false);
+  hcr_status st = validate_restore(h, a, &empty, /*stats=*/false, what);
   if (st != HCR_OK || empty) return st;
   void* dense = nullptr;
   st = device_view(h->impl, const_cast<void*>(a.hidden), what, &dense);

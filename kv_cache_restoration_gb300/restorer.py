@@ -103,6 +103,96 @@ class Restorer:
               "project": B.hcr_restore_project}[stage]
         return fn(*args, stream, check=check)
 
+    # --- the other entry points: thin wrappers that own staging buffers ----
+    def _stream(self, stream):
+        return torch.cuda.current_stream() if stream is None else stream
+
+    def _staging(self, nbytes: int, device) -> torch.Tensor:
+        st = getattr(self, "_stage_buf", None)
+        if st is None or st.numel() < nbytes or st.device != torch.device(device):
+            self._stage_buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        return self._stage_buf
+
+    def restore_streamed(self, hidden_host, layer_begin, layer_end, cu_seqlens, start_pos,
+                         block_table, k_cache, v_cache, num_blocks, block_size,
+                         layers_per_chunk: int = 4, slots: int = 3, layer_stride_elems=0,
+                         stream=None) -> int:
+        """Layer-pipelined restore from hidden states in (pinned) host memory,
+        [layer_end-layer_begin][T][d]."""
+        if hidden_host.is_cuda:
+            raise ValueError("hidden_host must be in host memory")
+        dev = k_cache.device
+        T, d = int(hidden_host.shape[-2]), self.dims.d_model
+        c = max(1, min(layers_per_chunk, layer_end - layer_begin))
+        staging = self._staging(slots * c * T * d * 2, dev)
+        ws = self.workspace(T, c, dev)
+        return B.hcr_restore_streamed(
+            self.handle, hidden_host, layer_begin, layer_end, int(start_pos.numel()), T,
+            cu_seqlens, start_pos, block_table, int(block_table.shape[-1]), k_cache, v_cache,
+            B.hcr_cache_layout(num_blocks, block_size, layer_stride_elems), staging,
+            staging.numel(), layers_per_chunk, ws, ws.numel(), self._stream(stream))
+
+    def save_hidden(self, hidden, layer_begin, layer_end, cu_seqlens, start_pos, chunk_table,
+                    chunk_tokens, chunk_store, stream=None) -> int:
+        """Layer inputs into a chunk store [num_chunks][n_layers][chunk_tokens][d]
+        (device or pinned host memory)."""
+        return B.hcr_save_hidden(self.handle, hidden, layer_begin, layer_end,
+                                 int(start_pos.numel()), int(hidden.shape[-2]), cu_seqlens,
+                                 start_pos, chunk_table, int(chunk_table.shape[-1]),
+                                 chunk_tokens, chunk_store, int(chunk_store.shape[0]),
+                                 self._stream(stream))
+
+    def _kv(self, fn, kv, layer_begin, layer_end, cu_seqlens, start_pos, block_table, k_cache,
+            v_cache, num_blocks, block_size, layer_stride_elems, stream):
+        T = int(kv.shape[-2])
+        ws = self.workspace(T, 1, k_cache.device)
+        return fn(self.handle, kv, layer_begin, layer_end, int(start_pos.numel()), T, cu_seqlens,
+                  start_pos, block_table, int(block_table.shape[-1]), k_cache, v_cache,
+                  B.hcr_cache_layout(num_blocks, block_size, layer_stride_elems), ws, ws.numel(),
+                  self._stream(stream))
+
+    def save_kv(self, kv, layer_begin, layer_end, cu_seqlens, start_pos, block_table, k_cache,
+                v_cache, num_blocks, block_size, layer_stride_elems=0, stream=None) -> int:
+        """K/V rows out of the paged cache into kv [layers][2][T][d_kv]."""
+        return self._kv(B.hcr_save_kv, kv, layer_begin, layer_end, cu_seqlens, start_pos,
+                        block_table, k_cache, v_cache, num_blocks, block_size,
+                        layer_stride_elems, stream)
+
+    def load_kv(self, kv, layer_begin, layer_end, cu_seqlens, start_pos, block_table, k_cache,
+                v_cache, num_blocks, block_size, layer_stride_elems=0, stream=None) -> int:
+        """K/V rows kv [layers][2][T][d_kv] back into the paged cache."""
+        return self._kv(B.hcr_load_kv, kv, layer_begin, layer_end, cu_seqlens, start_pos,
+                        block_table, k_cache, v_cache, num_blocks, block_size,
+                        layer_stride_elems, stream)
+
+    def encode(self, hidden, layer_begin, layer_end, cu_seqlens, n_req, codes=None, scales=None,
+               bins=(0.5, 1.0, 1.5), group_tokens: int = 10, stream=None):
+        """Hidden-state codec: returns (codes int8 [Lr][T][d], scales float32 [Lr][T])."""
+        Lr, T, d = (int(x) for x in hidden.shape)
+        if codes is None:
+            codes = torch.empty((Lr, T, d), dtype=torch.int8, device=hidden.device)
+        if scales is None:
+            scales = torch.zeros((Lr, T), dtype=torch.float32, device=hidden.device)
+        B.hcr_encode_hidden(self.handle, B.codec_params(bins, group_tokens), hidden, layer_begin,
+                            layer_end, n_req, T, cu_seqlens, codes, scales, self._stream(stream))
+        return codes, scales
+
+    def decode(self, codes, scales, layer_begin, layer_end, cu_seqlens, n_req, out=None,
+               bins=(0.5, 1.0, 1.5), group_tokens: int = 10, stream=None):
+        """Inverse of encode, into the storage dtype."""
+        if out is None:
+            out = torch.empty(tuple(codes.shape), dtype=self.torch_dtype, device=codes.device)
+        B.hcr_decode_hidden(self.handle, B.codec_params(bins, group_tokens), codes, scales,
+                            layer_begin, layer_end, n_req, int(codes.shape[-2]), cu_seqlens, out,
+                            self._stream(stream))
+        return out
+
+    def plan_split(self, n_tokens: int, layers_per_chunk: int = 4, reps: int = 5, stream=None):
+        """Profiles the per-layer costs on this GPU and returns (costs, split)."""
+        costs = B.hcr_profile_layer_costs(self.handle, n_tokens, layers_per_chunk, reps,
+                                          self._stream(stream))
+        return costs, B.hcr_plan_layer_split(costs, self.dims.n_layers)
+
     def check(self, stream=None):
         if stream is None:
             stream = torch.cuda.current_stream()

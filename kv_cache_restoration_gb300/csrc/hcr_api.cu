@@ -236,11 +236,16 @@ hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
   //     outweighs the lower rate;
   //   * single CTAs for models wider than 4096: at d_model 5120 and 7168 they
   //     ran 4-5% faster in long power-capped restores and no slower at
-  //     2-4K tokens, while at 4096 pairs win by 5-7%.
+  //     2-4K tokens, while at 4096 pairs win by 5-7%;
+  //   * single CTAs for calls of more than 32 TFLOP: pairs draw more power per
+  //     clock, and in long calls the power cap pulls their clock further down
+  //     (a 629K-token batch in 8-layer calls of 338 TFLOP: single CTAs 10%
+  //     faster; 35 TFLOP calls: a tie; 8.8 TFLOP calls: pairs 5.5% faster).
   const int64_t pad256 = (int64_t(a.n_tokens) + 2 * kBlockM - 1) / (2 * kBlockM) * (2 * kBlockM);
   const int64_t pad128 = (int64_t(a.n_tokens) + kBlockM - 1) / kBlockM * kBlockM;
+  const double call_flops = 4.0 * d.d_model * d_kv * double(a.n_tokens) * nl;
   bool pair = H.pair_clusters > 0 && a.n_tokens > kBlockM && d.d_model <= 4096 &&
-              10 * pad128 > 9 * pad256;
+              10 * pad128 > 9 * pad256 && call_flops <= 32e12;
   if (H.variant == 1) pair = false;
   if (H.variant == 2) pair = H.pair_clusters > 0;
   const int tile_m = pair ? 2 * kBlockM : kBlockM;

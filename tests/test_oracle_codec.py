@@ -175,3 +175,24 @@ def test_reciprocal_step_differs_from_division_only_by_rounding():
         assert np.abs(a - d).max() <= 1
         if b in (0.5, 1.0):           # power-of-two steps: identical
             assert np.array_equal(a, d)
+
+
+def test_defaults_are_the_pages_parameters():
+    """The oracle's and the library binding's codec defaults, and the save
+    side's chunk size used throughout, are the values the pages print
+    (tests/golden/page_parameters.json, each with its citation)."""
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "page_parameters.json")) as f:
+        g = json.load(f)
+    assert K.GROUP_TOKENS == g["codec"]["group_tokens"]
+    assert tuple(K.DEFAULT_BINS) == tuple(g["codec"]["bins_first_middle_last"])
+    # 8-bit symmetric anchors: codes span [-(2^7 - 1), 2^7 - 1]
+    q, _ = K.quantise_anchor(np.array([1.0, -1.0, 0.5], F32))
+    assert q.max() == 2 ** (g["codec"]["anchor_bits"] - 1) - 1
+    assert q.min() == -(2 ** (g["codec"]["anchor_bits"] - 1) - 1)
+    from kv_cache_restoration_gb300 import binding as B
+    p = B.codec_params()
+    assert list(p.bins) == g["codec"]["bins_first_middle_last"]
+    assert p.group_tokens == g["codec"]["group_tokens"]
+    assert g["save_chunk_tokens"]["value"] == 64

@@ -616,13 +616,87 @@ def codec_arm(args):
     print(json.dumps(line))
 
 
+def kv_arm(args):
+    """KV offload rows: every layer's K and V rows of the request out of the
+    paged cache (hcr_save_kv) and back (hcr_load_kv), device-resident store."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__._build_module().build()
+    from kv_cache_restoration_gb300 import Restorer, make_dims
+    from kv_cache_restoration_gb300 import binding as B
+    from workloads import configs as C
+    from workloads import generate as G
+
+    device = torch.device("cuda", 0)
+    w = C.get(args.workload)
+    if args.layers:
+        w = C.with_layers(w, args.layers)
+    s = w.shape
+    L, T = s.n_layers, w.n_tokens
+    d_kv = s.n_kv_heads * s.head_dim
+    case = G.device_inputs(w, device, gen_device=device)
+    r = Restorer(make_dims(L, s.d_model, s.n_heads, s.n_kv_heads, s.head_dim, s.norm,
+                           s.norm_eps, s.rope, s.rope_theta, w.rope_positions, s.dtype,
+                           s.kv_bias), case.params)
+    case.params = None
+    stream = torch.cuda.current_stream(device)
+    peaks, peak_kind = load_peaks()
+    lay = case.layout
+    layout = B.hcr_cache_layout(lay.num_blocks, lay.block_size, 0)
+    ws = r.workspace(T, 1, device)
+    kv = torch.empty((L, 2, T, d_kv), dtype=case.hidden.dtype, device=device)
+    r.restore(case.hidden, 0, L, case.cu, case.start, case.table, case.k_cache, case.v_cache,
+              lay.num_blocks, lay.block_size, stream=stream)
+
+    def call(fn):
+        return lambda: fn(r.handle, kv, 0, L, w.n_req, T, case.cu, case.start, case.table,
+                          lay.max_blocks, case.k_cache, case.v_cache, layout, ws, ws.numel(),
+                          stream)
+
+    def timed(fn, steps, warmup):
+        for _ in range(warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        if r.check(stream)[0] != 0:
+            raise RuntimeError("K/V rows reported a device error")
+        return e0.elapsed_time(e1) / 1e3 / steps
+
+    t_save = timed(call(B.hcr_save_kv), args.steps, args.warmup)
+    t_load = timed(call(B.hcr_load_kv), args.steps, args.warmup)
+    moved = 2.0 * L * 2 * T * d_kv * 2          # K and V rows, read once and written once
+    line = {
+        "op": "kv", "metric": "K/V rows placed per second (hcr_load_kv, all layers)",
+        "value": T / t_load, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_load * 1e3, "higher_is_better": True,
+        "dtype": s.dtype, "data": "synthetic",
+        "config": {"workload": f"{w.name}: {L} layers x {T} tokens x d_kv={d_kv}, "
+                               f"block {w.block_size} ({w.block_order})"},
+        "roofline": {"bound": "hbm", "achieved": moved / t_load / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": moved / t_load / 1e9 / peaks["hbm_gbs"],
+                     "peak_source": f"{peak_kind} HBM copy bandwidth",
+                     "kernel": "kv_rows_kernel (plus the placement-only prepare_kernel)"},
+        "save": {"ms_per_step": t_save * 1e3, "achieved_gbs": moved / t_save / 1e9,
+                 "frac": moved / t_save / 1e9 / peaks["hbm_gbs"]},
+        "gpu_launches": 2 * args.steps,
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--op", default="restore", choices=["restore", "save", "codec"],
+    ap.add_argument("--op", default="restore", choices=["restore", "save", "codec", "kv"],
                     help="restore (the benchmark step) or save (hcr_save_hidden)")
     ap.add_argument("--workload", default="llama2-7b")
     ap.add_argument("--e2e-steps", type=int, default=30, help="0 skips the end-to-end leg")
@@ -659,6 +733,8 @@ def main():
         return save_arm(args)
     if args.op == "codec":
         return codec_arm(args)
+    if args.op == "kv":
+        return kv_arm(args)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

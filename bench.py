@@ -423,6 +423,10 @@ def gpu_arm(args, rank, world, local_rank):
         torch.cuda.synchronize(device)
         h2d_gbs = hidden_host.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9
 
+    torch_ctx = None
+    if args.torch_context and nw == 1:
+        torch_ctx = torch_composite_ms(w, case, device, stream)
+
     t_step = total_ms / 1e3 / args.steps
     e2e_med = statistics.median(step_s) if step_s else float("nan")
     e2e_p90 = sorted(step_s)[int(0.9 * (len(step_s) - 1))] if step_s else float("nan")
@@ -432,8 +436,67 @@ def gpu_arm(args, rank, world, local_rank):
     return dict(w=w, t_step=t_step, proj_ms=proj_ms, prep_ms=prep_ms, e2e_s=e2e_s, h2d=h2d,
                 clocks=clk.summary(), launches=2 * nw * args.steps, windows=windows,
                 h2d_gbs=h2d_gbs, chunk=chunk,
-                split=split_plan,
+                split=split_plan, torch_ctx=torch_ctx,
                 e2e_median_s=e2e_med, e2e_p90_s=e2e_p90, e2e_max_s=e2e_max)
+
+
+def torch_composite_ms(w, case, device, stream, reps: int = 3):
+    """Context only: the same restore written as PyTorch ops on this GPU (norm
+    in fp32, a cuBLAS GEMM in the storage dtype, RoPE in fp32, an indexed
+    scatter into the paged cache), timed with CUDA events after the library's
+    own measurements.  It shares nothing with the library's path."""
+    import numpy as np
+    import torch
+
+    from workloads import generate as G
+    s = w.shape
+    L, T, dh = s.n_layers, w.n_tokens, s.head_dim
+    d_kv = s.n_kv_heads * dh
+    dt = G.TORCH_DTYPE[s.dtype]
+    lay = case.layout
+    params = [G.layer_params(s, l, w.seed, device) for l in range(L)]
+    w_cat = [torch.cat([p.w_k, p.w_v]) for p in params]
+    cu, start, bt = lay.cu_seqlens, lay.start_pos, lay.block_table
+    pos = np.concatenate([start[r] + np.arange(cu[r + 1] - cu[r]) for r in range(len(start))])
+    req = np.concatenate([np.full(cu[r + 1] - cu[r], r) for r in range(len(start))])
+    slot = torch.as_tensor(bt[req, pos // w.block_size] * w.block_size + pos % w.block_size,
+                           device=device)
+    if s.rope:
+        inv = torch.tensor(s.rope_theta, dtype=torch.float64) ** (
+            -torch.arange(0, dh, 2, dtype=torch.float64) / dh)
+        ang = (torch.as_tensor(pos, dtype=torch.float64)[:, None] * inv[None, :]).to(device)
+        cos, sin = ang.cos().float()[:, None, :], ang.sin().float()[:, None, :]
+
+    def one():
+        for l in range(L):
+            x = case.hidden[l].float()
+            p = params[l]
+            if s.norm == "ln":
+                mu = x.mean(-1, keepdim=True)
+                xn = (x - mu) * torch.rsqrt((x - mu).pow(2).mean(-1, keepdim=True) + s.norm_eps)
+                xn = xn * p.gamma.float() + p.beta.float()
+            else:
+                xn = x * torch.rsqrt(x.pow(2).mean(-1, keepdim=True) + s.norm_eps) * p.gamma.float()
+            y = xn.to(dt) @ w_cat[l].t()
+            if p.b_k is not None:
+                y = y + torch.cat([p.b_k, p.b_v])
+            k, v = y[:, :d_kv], y[:, d_kv:]
+            if s.rope:
+                kf = k.float().view(T, s.n_kv_heads, dh)
+                a, b = kf[..., :dh // 2], kf[..., dh // 2:]
+                k = torch.cat([a * cos - b * sin, b * cos + a * sin], -1).view(T, d_kv).to(dt)
+            case.k_cache[l].view(-1, d_kv)[slot] = k
+            case.v_cache[l].view(-1, d_kv)[slot] = v
+
+    with torch.cuda.stream(stream):
+        one()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            one()
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    return e0.elapsed_time(e1) / reps
 
 
 def save_arm(args):
@@ -717,6 +780,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="cut the model to its first N layers (small profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--torch-context", type=int, default=1,
+                    help="1: also time the restore written as PyTorch ops (context only)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per project launch from an ncu capture")
     ap.add_argument("--oracle-child", action="store_true")
@@ -865,6 +930,12 @@ def main():
                 if res["e2e_s"] == res["e2e_s"] else None),
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
+        "context": ({"torch_composite_ms_per_step": res["torch_ctx"],
+                     "library_speedup": res["torch_ctx"] / (t * 1e3),
+                     "note": "the same restore as PyTorch ops on this GPU (fp32 norm, cuBLAS "
+                             "GEMM, fp32 RoPE, indexed scatter), timed after the library's "
+                             "legs; context only, not a target"}
+                    if res.get("torch_ctx") else None),
     }
     print(json.dumps(line))
 

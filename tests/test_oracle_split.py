@@ -150,3 +150,21 @@ def test_c_planner_rejects_bad_costs(bad):
     assert e.value.status == B.HCR_ERR_INVALID_ARG
     with pytest.raises(B.HcrError):
         B.hcr_plan_layer_split(B.hcr_layer_costs(1, 1, 1, 1), -1)
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_meet_in_the_middle_closed_form(seed):
+    """CacheFlow episode, cue 12: with one method costing only compute (r per
+    layer) and the other only transfer (kc per layer), splitting so both
+    finish together takes L * r * kc / (r + kc) -- the product over the sum
+    of the two per-layer costs.  The planner reduces to that case when the
+    hidden-state transfer and the K/V placement cost nothing; the integer
+    split is within one layer's cost of it and never below it."""
+    rng = random.Random(100 + seed)
+    r, kc = rng.uniform(0.1, 3.0), rng.uniform(0.1, 3.0)
+    L = rng.randint(1, 120)
+    s = SP.plan_layer_split(SP.LayerCosts(r, 0.0, kc, 0.0), L)
+    t_star = L * r * kc / (r + kc)
+    assert t_star - 1e-12 <= s.predicted <= t_star + max(r, kc)
+    # and the split itself sits where the two totals cross
+    assert abs(s.kv_layers - L * r / (r + kc)) <= 1

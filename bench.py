@@ -762,7 +762,7 @@ def main():
     ap.add_argument("--op", default="restore", choices=["restore", "save", "codec", "kv"],
                     help="restore (the benchmark step) or save (hcr_save_hidden)")
     ap.add_argument("--workload", default="llama2-7b")
-    ap.add_argument("--e2e-steps", type=int, default=30, help="0 skips the end-to-end leg")
+    ap.add_argument("--e2e-steps", type=int, default=100, help="0 skips the end-to-end leg")
     ap.add_argument("--e2e-chunk", type=int, default=4, help="layers per streamed chunk")
     ap.add_argument("--e2e-slots", type=int, default=3, help="staging ring slots")
     ap.add_argument("--e2e-source", default="layers",

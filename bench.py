@@ -437,6 +437,7 @@ def gpu_arm(args, rank, world, local_rank):
                 clocks=clk.summary(), launches=2 * nw * args.steps, windows=windows,
                 h2d_gbs=h2d_gbs, chunk=chunk,
                 split=split_plan, torch_ctx=torch_ctx,
+                variant=B.hcr_project_variant(r.handle, T, windows[0][1] - windows[0][0]),
                 e2e_median_s=e2e_med, e2e_p90_s=e2e_p90, e2e_max_s=e2e_max)
 
 
@@ -893,7 +894,8 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": s.dtype, "data": "synthetic",
         "config": {"workload": workload_desc,
-                   "project_variant": {0: "auto", 1: "single", 2: "pair"}[args.variant],
+                   "project_variant": ({0: "auto", 1: "single", 2: "pair"}[args.variant]
+                                       + f" -> {({1: 'single CTAs', 2: 'CTA pairs'}).get(res['variant'], '?')}"),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2 ({(hid_b + w_b + kv_b) / 1e9:.2f} GB "
                          "moved per step vs 129 MB L2); no flush",

@@ -500,6 +500,18 @@ hcr_status hcr_restore_no_alloc(hcr_handle* h, const void* hidden, int32_t layer
  * HCR_ERR_TIMEOUT (timeout wins), or HCR_ERR_CUDA if the synchronisation
  * failed.  The raw HCR_DEVERR_* bits go to *flags when flags is not NULL.
  */
+/*
+ * hcr_project_variant -- the tile variant the projection of n_tokens tokens
+ * over n_layers layers uses: 1 for single CTAs (128x256 tiles), 2 for CTA
+ * pairs (256x256 tiles, cta_group::2).  Host-only; 0 for a NULL handle or
+ * empty sizes.  The choice, made from measurements on GB300: pairs when
+ * there is more than one 128-row tile of tokens, d_model <= 4096, padding to
+ * 128-row tiles saves less than 10% of the rows that 256-row tiles pad, and
+ * the call is at most 32 TFLOP (4 d_model d_kv n_tokens n_layers); single
+ * CTAs otherwise.  hcr_debug_set_variant overrides it.
+ */
+int32_t hcr_project_variant(const hcr_handle* h, int32_t n_tokens, int32_t n_layers);
+
 hcr_status hcr_check_device_error(hcr_handle* h, void* stream, uint32_t* flags);
 
 /*

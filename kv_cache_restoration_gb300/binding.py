@@ -146,6 +146,8 @@ lib.hcr_status_string.argtypes = [ctypes.c_int]
 lib.hcr_status_string.restype = ctypes.c_char_p
 lib.hcr_last_error.argtypes = []
 lib.hcr_last_error.restype = ctypes.c_char_p
+lib.hcr_project_variant.argtypes = [_vp, _i32, _i32]
+lib.hcr_project_variant.restype = _i32
 lib.hcr_num_sms.argtypes = [_vp]
 lib.hcr_num_sms.restype = _i32
 lib.hcr_debug_timeout_record.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -421,6 +423,11 @@ def hcr_check_device_error(handle, stream=None):
     flags = ctypes.c_uint32(0)
     st = lib.hcr_check_device_error(handle, _stream_ptr(stream), ctypes.byref(flags))
     return st, flags.value
+
+
+def hcr_project_variant(handle, n_tokens: int, n_layers: int) -> int:
+    """Tile variant the projection uses: 1 single CTAs, 2 CTA pairs (host-only)."""
+    return lib.hcr_project_variant(handle, n_tokens, n_layers)
 
 
 def hcr_num_sms(handle) -> int:

@@ -203,6 +203,37 @@ hcr_status do_prepare(hcr_handle* h, const RestoreArgs& a, bool stats = true) {
   return HCR_OK;
 }
 
+// Tile variant of a projection of n_tokens tokens over n_layers layers
+// (true: CTA pairs), chosen from measurements on GB300:
+//   * CTA pairs (256-row tiles) once there is more than one 128-row tile of
+//     tokens: they do ~8-12% more work per clock, and weight-streaming
+//     restores of 129-256 tokens run ~15% faster with them;
+//   * single CTAs for short restores (one 128-row tile of tokens), which
+//     would only pad the pair's second half;
+//   * single CTAs where 128-row tiles pad at least 10% fewer rows than
+//     256-row tiles (e.g. 300, 640 or 794 tokens): the padding saved
+//     outweighs the lower rate;
+//   * single CTAs for models wider than 4096: at d_model 5120 and 7168 they
+//     ran 4-5% faster in long power-capped restores and no slower at
+//     2-4K tokens, while at 4096 pairs win by 5-7%;
+//   * single CTAs for calls of more than 32 TFLOP: pairs draw more power per
+//     clock, and in long calls the power cap pulls their clock further down
+//     (a 629K-token batch in 8-layer calls of 338 TFLOP: single CTAs 10%
+//     faster; 35 TFLOP calls: a tie; 8.8 TFLOP calls: pairs 5.5% faster).
+// The debug hook (hcr_debug_set_variant) overrides the choice.
+bool use_pairs(const Handle& H, int32_t n_tokens, int32_t n_layers) {
+  const hcr_model_dims& d = H.dims;
+  const int64_t d_kv = int64_t(d.n_kv_heads) * d.head_dim;
+  const int64_t pad256 = (int64_t(n_tokens) + 2 * kBlockM - 1) / (2 * kBlockM) * (2 * kBlockM);
+  const int64_t pad128 = (int64_t(n_tokens) + kBlockM - 1) / kBlockM * kBlockM;
+  const double call_flops = 4.0 * d.d_model * double(d_kv) * double(n_tokens) * n_layers;
+  bool pair = H.pair_clusters > 0 && n_tokens > kBlockM && d.d_model <= 4096 &&
+              10 * pad128 > 9 * pad256 && call_flops <= 32e12;
+  if (H.variant == 1) pair = false;
+  if (H.variant == 2) pair = H.pair_clusters > 0;
+  return pair;
+}
+
 hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
   NvtxRange range("hcr.project");
   const Handle& H = h->impl;
@@ -225,29 +256,7 @@ hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
   p.head_dim = d.head_dim;
   p.n_layers = nl;
   p.layer_begin = a.layer_begin;
-  // Tile variant, chosen from measurements on GB300:
-  //   * CTA pairs (256-row tiles) once there is more than one 128-row tile of
-  //     tokens: they do ~8-12% more work per clock, and weight-streaming
-  //     restores of 129-256 tokens run ~15% faster with them;
-  //   * single CTAs for short restores (one 128-row tile of tokens), which
-  //     would only pad the pair's second half;
-  //   * single CTAs where 128-row tiles pad at least 10% fewer rows than
-  //     256-row tiles (e.g. 300, 640 or 794 tokens): the padding saved
-  //     outweighs the lower rate;
-  //   * single CTAs for models wider than 4096: at d_model 5120 and 7168 they
-  //     ran 4-5% faster in long power-capped restores and no slower at
-  //     2-4K tokens, while at 4096 pairs win by 5-7%;
-  //   * single CTAs for calls of more than 32 TFLOP: pairs draw more power per
-  //     clock, and in long calls the power cap pulls their clock further down
-  //     (a 629K-token batch in 8-layer calls of 338 TFLOP: single CTAs 10%
-  //     faster; 35 TFLOP calls: a tie; 8.8 TFLOP calls: pairs 5.5% faster).
-  const int64_t pad256 = (int64_t(a.n_tokens) + 2 * kBlockM - 1) / (2 * kBlockM) * (2 * kBlockM);
-  const int64_t pad128 = (int64_t(a.n_tokens) + kBlockM - 1) / kBlockM * kBlockM;
-  const double call_flops = 4.0 * d.d_model * d_kv * double(a.n_tokens) * nl;
-  bool pair = H.pair_clusters > 0 && a.n_tokens > kBlockM && d.d_model <= 4096 &&
-              10 * pad128 > 9 * pad256 && call_flops <= 32e12;
-  if (H.variant == 1) pair = false;
-  if (H.variant == 2) pair = H.pair_clusters > 0;
+  const bool pair = use_pairs(H, a.n_tokens, nl);
   const int tile_m = pair ? 2 * kBlockM : kBlockM;
   p.m_tiles = (a.n_tokens + tile_m - 1) / tile_m;
   p.n_tiles = (2 * d_kv + kBlockN - 1) / kBlockN;
@@ -557,6 +566,11 @@ hcr_status hcr_save_kv(hcr_handle* h, void* kv, int32_t layer_begin, int32_t lay
                 const_cast<void*>(v_cache), layout, workspace, workspace_bytes,
                 static_cast<cudaStream_t>(stream)};
   return kv_rows(h, a, /*to_cache=*/false, "kv");
+}
+
+int32_t hcr_project_variant(const hcr_handle* h, int32_t n_tokens, int32_t n_layers) {
+  if (!h || n_tokens <= 0 || n_layers <= 0) return 0;
+  return use_pairs(h->impl, n_tokens, n_layers) ? 2 : 1;
 }
 
 hcr_status hcr_check_device_error(hcr_handle* h, void* stream, uint32_t* flags) {

@@ -273,3 +273,29 @@ def test_host_validation(cuda_device):
     # nothing was launched: the caches still hold only sentinels
     assert bool((case.k_cache.view(torch.int16) == G.SENTINEL_BITS).all())
     assert call() == B.HCR_OK
+
+
+def test_variant_policy_decisions(cuda_device):
+    """The automatic tile variant on the cases it was measured on."""
+    from kv_cache_restoration_gb300 import Restorer, binding as B, make_dims
+    from workloads import generate as G
+    from workloads.configs import LLAMA2_7B, LLAMA2_13B
+
+    def handle(shape):
+        # a 1-layer handle of the shape: the policy reads dims, not weights
+        params = [G.layer_params(shape, 0, 0, cuda_device)]
+        return Restorer(make_dims(1, shape.d_model, shape.n_heads, shape.n_kv_heads,
+                                  shape.head_dim, shape.norm, shape.norm_eps, shape.rope,
+                                  shape.rope_theta, 16384, shape.dtype, shape.kv_bias), params)
+    r7 = handle(LLAMA2_7B)
+    h = r7.handle
+    want = {(64, 32): 1, (128, 32): 1, (256, 32): 2, (300, 32): 1, (500, 32): 2, (794, 32): 1,
+            (4096, 32): 2, (4096, 4): 2, (16384, 32): 1, (629259, 8): 1}
+    assert {k: B.hcr_project_variant(h, *k) for k in want} == want
+    assert B.hcr_project_variant(h, 0, 32) == 0
+    assert B.hcr_debug_set_variant(h, 2) == 0
+    assert B.hcr_project_variant(h, 300, 32) == 2
+    assert B.hcr_debug_set_variant(h, 1) == 0
+    assert B.hcr_project_variant(h, 4096, 32) == 1
+    r13 = handle(LLAMA2_13B)
+    assert B.hcr_project_variant(r13.handle, 4096, 40) == 1     # d_model 5120

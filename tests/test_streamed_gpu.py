@@ -91,3 +91,16 @@ def test_streamed_rejects_small_buffers(cuda_device):
     torch.cuda.synchronize()
     from workloads import generate as G
     assert bool((case.k_cache.view(torch.int16) == G.SENTINEL_BITS).all())
+
+
+def test_streamed_full_size_13b(cuda_device):
+    """Llama2-13B shape, 16384 tokens, shuffled blocks: the single-CTA tiles
+    (chosen for d_model > 4096) through the streamed pipeline at full size."""
+    w = C.get("llama2-13b")
+    ref = Hn.run(Hn.make_case(w, cuda_device, gen_device=cuda_device))
+    assert ref.status == 0
+    case = Hn.make_case(w, cuda_device, params=ref.params, restorer=ref.restorer,
+                        gen_device=cuda_device)
+    assert _streamed(case, 4, 3) == 0
+    assert case.restorer.check()[0] == 0
+    _same(case, ref)

@@ -210,9 +210,10 @@ hcr_status do_prepare(hcr_handle* h, const RestoreArgs& a, bool stats = true) {
 //     restores of 129-256 tokens run ~15% faster with them;
 //   * single CTAs for short restores (one 128-row tile of tokens), which
 //     would only pad the pair's second half;
-//   * single CTAs where 128-row tiles pad at least 10% fewer rows than
-//     256-row tiles (e.g. 300, 640 or 794 tokens): the padding saved
-//     outweighs the lower rate;
+//   * single CTAs where 128-row tiles pad at least 10% fewer rows than the
+//     pairs' tiles: the padding saved outweighs the lower rate.  With the
+//     half tail (below) pairs pad no more than single CTAs unless heads are
+//     wider than 128 columns;
 //   * single CTAs for models wider than 4096: at d_model 5120 and 7168 they
 //     ran 4-5% faster in long power-capped restores and no slower at
 //     2-4K tokens, while at 4096 pairs win by 5-7%;
@@ -221,14 +222,26 @@ hcr_status do_prepare(hcr_handle* h, const RestoreArgs& a, bool stats = true) {
 //     (a 629K-token batch in 8-layer calls of 338 TFLOP: single CTAs 10%
 //     faster; 35 TFLOP calls: a tie; 8.8 TFLOP calls: pairs 5.5% faster).
 // The debug hook (hcr_debug_set_variant) overrides the choice.
+// A pair projection can end each layer with an M=128 "half tail" tile (64
+// rows per CTA) when the last 256-row tile holds at most 128 rows; its
+// epilogue splits a row's 256 columns in two 128-column halves, so heads must
+// fit in 128 columns.
+bool half_tail_fits(const hcr_model_dims& d, int32_t n_tokens) {
+  const int32_t rem = n_tokens % (2 * kBlockM);
+  return d.head_dim <= kBlockN / 2 && rem > 0 && rem <= kBlockM;
+}
+
 bool use_pairs(const Handle& H, int32_t n_tokens, int32_t n_layers) {
   const hcr_model_dims& d = H.dims;
   const int64_t d_kv = int64_t(d.n_kv_heads) * d.head_dim;
-  const int64_t pad256 = (int64_t(n_tokens) + 2 * kBlockM - 1) / (2 * kBlockM) * (2 * kBlockM);
+  // rows each variant computes: 128-row tiles, or 256-row tiles whose last
+  // tile may be a 128-row half tail
   const int64_t pad128 = (int64_t(n_tokens) + kBlockM - 1) / kBlockM * kBlockM;
+  const int64_t pad_pair = (int64_t(n_tokens) + 2 * kBlockM - 1) / (2 * kBlockM) * (2 * kBlockM) -
+                           (half_tail_fits(d, n_tokens) ? kBlockM : 0);
   const double call_flops = 4.0 * d.d_model * double(d_kv) * double(n_tokens) * n_layers;
   bool pair = H.pair_clusters > 0 && n_tokens > kBlockM && d.d_model <= 4096 &&
-              10 * pad128 > 9 * pad256 && call_flops <= 32e12;
+              10 * pad128 > 9 * pad_pair && call_flops <= 32e12;
   if (H.variant == 1) pair = false;
   if (H.variant == 2) pair = H.pair_clusters > 0;
   return pair;
@@ -258,6 +271,7 @@ hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
   p.layer_begin = a.layer_begin;
   const bool pair = use_pairs(H, a.n_tokens, nl);
   const int tile_m = pair ? 2 * kBlockM : kBlockM;
+  p.half_tail = pair && half_tail_fits(d, a.n_tokens);
   p.m_tiles = (a.n_tokens + tile_m - 1) / tile_m;
   p.n_tiles = (2 * d_kv + kBlockN - 1) / kBlockN;
   p.k_blocks = (d.d_model + kBlockK - 1) / kBlockK;
@@ -284,8 +298,14 @@ hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
   p.debug_stall = H.debug_stall;
   const int grid = pair ? 2 * int(std::min<int64_t>(p.num_tiles, H.pair_clusters))
                         : int(std::min<int64_t>(p.num_tiles, H.num_sms));
-  cudaError_t e =
-      launch_project(tmap_h, pair ? H.tmap_w_half : H.tmap_w, p, grid, pair, a.stream);
+  CUtensorMap tmap_h64 = tmap_h;
+  if (p.half_tail) {
+    st = encode_3d(&tmap_h64, a.hidden, d.dtype, uint64_t(d.d_model), uint64_t(a.n_tokens),
+                   uint64_t(nl), kBlockM / 2, "hidden (64-row boxes)");
+    if (st != HCR_OK) return st;
+  }
+  cudaError_t e = launch_project(tmap_h, tmap_h64, pair ? H.tmap_w_half : H.tmap_w, p, grid,
+                                 pair, a.stream);
   if (e != cudaSuccess) return cuda_fail(e, "project launch");
   return HCR_OK;
 }

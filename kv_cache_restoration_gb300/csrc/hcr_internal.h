@@ -105,6 +105,9 @@ struct PrepareParams {
 struct ProjectParams {
   int32_t n_tokens, d_model, n_cols, d_kv, head_dim, n_layers, layer_begin;
   int32_t m_tiles, n_tiles, k_blocks;
+  // CTA pairs only: the last m-tile of each layer holds at most 128 rows and
+  // runs as an M=128 pair tile (64 rows per CTA) instead of a 256-row one.
+  int32_t half_tail;
   int64_t num_tiles;
   int32_t layer_norm, has_bias, rope, dtype;
   const int64_t* slot;
@@ -124,8 +127,10 @@ struct ProjectParams {
 
 // Launchers (return cudaGetLastError() of the launch).
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t s);
-cudaError_t launch_project(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
-                           const ProjectParams& p, int grid, bool pair, cudaStream_t s);
+// tmap_h64: the hidden states with 64-row boxes, read by half tail tiles.
+cudaError_t launch_project(const CUtensorMap& tmap_h, const CUtensorMap& tmap_h64,
+                           const CUtensorMap& tmap_w, const ProjectParams& p, int grid, bool pair,
+                           cudaStream_t s);
 // Co-resident clusters of the CTA-pair variant on the current device (< 0 on error).
 int project_pair_clusters(int dtype);
 cudaError_t launch_pack_weights(const void* w_k, const void* w_v, const void* gamma, void* dst,

@@ -27,8 +27,10 @@
 // Two variants: single CTAs with 128x256 tiles (cta_group::1, 4 stages of
 // 48 KB), and CTA pairs with 256x256 tiles (cta_group::2, 7 stages of 32 KB
 // per CTA).  The pair halves each SM's share of the weight tile, which cuts
-// shared-memory traffic per MMA by a third; the host picks the pair for
-// restores of more than 128 tokens.
+// shared-memory traffic per MMA by a third; the host picks the variant by
+// token count, width and call size.  A pair launch whose layers end in at most
+// 128 rows runs that last m-tile as an M=128 pair tile (64 rows per CTA), so
+// the pair pads no more rows than single CTAs do.
 // Every pipeline wait is bounded (kWaitLimitNs); on expiry the kernel sets
 // HCR_DEVERR_TIMEOUT, stops all roles, drains in-flight copies and MMAs with
 // a bounded wait, frees TMEM and returns.
@@ -153,9 +155,13 @@ struct Tiling {
   static constexpr int kStageBytes = kTileBytesA + kBytesB;
 };
 
-template <int DT, bool PAIR>
+// HT (pairs only): each layer's last m-tile is a half tail tile (M=128 across
+// the pair).  A separate instantiation, so the common kernel carries none of
+// its checks.
+template <int DT, bool PAIR, bool HT>
 __global__ void __launch_bounds__(kProjectThreads, 1)
     project_kernel(const __grid_constant__ CUtensorMap tmap_h,
+                   const __grid_constant__ CUtensorMap tmap_h64,
                    const __grid_constant__ CUtensorMap tmap_w, const ProjectParams p) {
   using Tl = Tiling<PAIR>;
   constexpr int S = Tl::kStages;
@@ -210,6 +216,7 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmap_h);
       ptx::tma_prefetch_desc(&tmap_w);
+      if (HT) ptx::tma_prefetch_desc(&tmap_h64);
       // A weight tile is read by every m-tile of its raster group: with several
       // m-tiles keep it in L2 ahead of other data (with one it is streamed
       // once and loaded without a hint).
@@ -220,7 +227,9 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
       bool ok = true;
       for (int64_t tile = unit; ok && tile < p.num_tiles; tile += units) {
         const TileCoord c = tile_coord(tile, p);
-        const int row_a = c.m * Tl::kTileM + int(rank) * kBlockM;
+        // a half tail tile stages 64 rows of A per CTA (M=128 across the pair)
+        const bool half_tile = HT && c.m == p.m_tiles - 1;
+        const int row_a = c.m * Tl::kTileM + int(rank) * (half_tile ? kBlockM / 2 : kBlockM);
         const int row_b = c.n * kBlockN + int(rank) * Tl::kRowsB;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase(ptx::smem_u32(&ps.empty[stage]), phase ^ 1u, abort, p, kWaitProducerEmpty,
@@ -234,10 +243,13 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
           if constexpr (PAIR) {
             // both CTAs' bytes complete on the leader's barrier; only the
             // leader arrives (with the pair's total byte count)
-            if (leader) ptx::mbar_arrive_expect_tx(full, 2 * Tl::kStageBytes);
+            if (leader)
+              ptx::mbar_arrive_expect_tx(
+                  full, half_tile ? 2 * (kTileBytesA / 2 + Tl::kBytesB) : 2 * Tl::kStageBytes);
             const uint32_t full_leader = ptx::mapa_shared(full, 0);
             if (!(p.debug_stall && issued == 0)) {
-              ptx::tma_load_3d_pair(dst_a, &tmap_h, full_leader, kb * kBlockK, row_a, c.l);
+              ptx::tma_load_3d_pair(dst_a, half_tile ? &tmap_h64 : &tmap_h, full_leader,
+                                    kb * kBlockK, row_a, c.l);
               if (reuse_w)
                 ptx::tma_load_3d_pair_hint(dst_b, &tmap_w, full_leader, kb * kBlockK, row_b,
                                            p.layer_begin + c.l, keep);
@@ -268,6 +280,7 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
       constexpr uint32_t idesc = make_idesc_f16(DT, Tl::kTileM, kBlockN);
+      constexpr uint32_t idesc_half = make_idesc_f16(DT, kBlockM, kBlockN);   // pairs, M=128
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -279,6 +292,8 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
           break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * kBlockN);
+        const uint32_t id =
+            (HT && tile_coord(tile, p).m == p.m_tiles - 1) ? idesc_half : idesc;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase(ptx::smem_u32(&ps.full[stage]), phase, abort, p, kWaitMmaFull,
                           uint32_t(tile), uint32_t(kb))) {
@@ -293,9 +308,9 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
             const uint64_t da = ptx::sw128_kmajor_desc(a0 + k * kUmmaK * 2);
             const uint64_t db = ptx::sw128_kmajor_desc(b0 + k * kUmmaK * 2);
             if constexpr (PAIR)
-              ptx::mma_f16_pair(d_tmem, da, db, idesc, (kb | k) != 0 ? 1u : 0u);
+              ptx::mma_f16_pair(d_tmem, da, db, id, (kb | k) != 0 ? 1u : 0u);
             else
-              ptx::mma_f16(d_tmem, da, db, idesc, (kb | k) != 0 ? 1u : 0u);
+              ptx::mma_f16(d_tmem, da, db, id, (kb | k) != 0 ? 1u : 0u);
           }
           if constexpr (PAIR)
             ptx::mma_commit_pair_multicast(ptx::smem_u32(&ps.empty[stage]), 0x3);
@@ -340,7 +355,15 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
       if (!ok) break;
       ptx::tc_fence_after();
 
-      const int t = c.m * Tl::kTileM + int(rank) * kBlockM + row;
+      // Full tile: TMEM lane `row` holds this CTA's token row `row`, all 256
+      // columns.  Half tail tile (pairs, M=128): lane L holds row L % 64 of this
+      // CTA's 64 rows, for the tile's columns 128 * (L / 64) .. +127, stored at
+      // TMEM columns 0..127 (the tcgen05 layout of a cta_group::2 M=128 MMA).
+      const bool half_tile = HT && c.m == p.m_tiles - 1;
+      const int col_lo = half_tile ? (row >> 6) * (kBlockN / 2) : 0;
+      const int col_hi = half_tile ? col_lo + kBlockN / 2 : kBlockN;
+      const int t = c.m * Tl::kTileM +
+                    (half_tile ? int(rank) * (kBlockM / 2) + (row & 63) : int(rank) * kBlockM + row);
       bool valid = t < p.n_tokens;
       int64_t slot = -1;
       int pos = 0;
@@ -357,7 +380,7 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
       const float* cbias = p.has_bias ? p.col_bias + int64_t(c.l) * p.n_cols : nullptr;
       const uint32_t tacc = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * kBlockN);
 
-      for (int h0 = 0; h0 < kBlockN; h0 += p.head_dim) {
+      for (int h0 = col_lo; h0 < col_hi; h0 += p.head_dim) {   // warp-uniform bounds
         const int col0 = c.n * kBlockN + h0;
         if (col0 >= p.n_cols) break;   // ragged last n-tile (warp-uniform)
         const bool is_k = col0 < p.d_kv;
@@ -371,8 +394,8 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
         const bool do_rope = is_k && p.rope;
         for (int j = 0; j < half; j += 16) {
           uint32_t ra[16], rb[16];
-          ptx::tmem_ld16(tacc + uint32_t(h0 + j), ra);
-          ptx::tmem_ld16(tacc + uint32_t(h0 + half + j), rb);
+          ptx::tmem_ld16(tacc + uint32_t(h0 - col_lo + j), ra);
+          ptx::tmem_ld16(tacc + uint32_t(h0 - col_lo + half + j), rb);
           ptx::tmem_ld_wait();
           float a[16], b[16];
           const int ca = col0 + j, cb = col0 + half + j;
@@ -465,10 +488,11 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
   }
 }
 
-template <int DT, bool PAIR>
-cudaError_t launch_variant(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
-                           const ProjectParams& p, int grid, cudaStream_t s) {
-  auto kernel = project_kernel<DT, PAIR>;
+template <int DT, bool PAIR, bool HT = false>
+cudaError_t launch_variant(const CUtensorMap& tmap_h, const CUtensorMap& tmap_h64,
+                           const CUtensorMap& tmap_w, const ProjectParams& p, int grid,
+                           cudaStream_t s) {
+  auto kernel = project_kernel<DT, PAIR, HT>;
   constexpr size_t smem = PAIR ? kSmemPair : kSmemSingle;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(smem));
@@ -487,12 +511,12 @@ cudaError_t launch_variant(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, kernel, tmap_h, tmap_w, p);
+  return cudaLaunchKernelEx(&cfg, kernel, tmap_h, tmap_h64, tmap_w, p);
 }
 
 template <int DT>
 int max_pair_clusters() {
-  auto kernel = project_kernel<DT, true>;
+  auto kernel = project_kernel<DT, true, false>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(kSmemPair)) != cudaSuccess)
     return -1;
@@ -517,13 +541,18 @@ int max_pair_clusters() {
 
 }  // namespace
 
-cudaError_t launch_project(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
-                           const ProjectParams& p, int grid, bool pair, cudaStream_t s) {
-  if (p.dtype == HCR_DTYPE_BF16)
-    return pair ? launch_variant<HCR_DTYPE_BF16, true>(tmap_h, tmap_w, p, grid, s)
-                : launch_variant<HCR_DTYPE_BF16, false>(tmap_h, tmap_w, p, grid, s);
-  return pair ? launch_variant<HCR_DTYPE_FP16, true>(tmap_h, tmap_w, p, grid, s)
-              : launch_variant<HCR_DTYPE_FP16, false>(tmap_h, tmap_w, p, grid, s);
+cudaError_t launch_project(const CUtensorMap& tmap_h, const CUtensorMap& tmap_h64,
+                           const CUtensorMap& tmap_w, const ProjectParams& p, int grid, bool pair,
+                           cudaStream_t s) {
+  const bool ht = pair && p.half_tail;
+  if (p.dtype == HCR_DTYPE_BF16) {
+    if (ht) return launch_variant<HCR_DTYPE_BF16, true, true>(tmap_h, tmap_h64, tmap_w, p, grid, s);
+    return pair ? launch_variant<HCR_DTYPE_BF16, true>(tmap_h, tmap_h64, tmap_w, p, grid, s)
+                : launch_variant<HCR_DTYPE_BF16, false>(tmap_h, tmap_h64, tmap_w, p, grid, s);
+  }
+  if (ht) return launch_variant<HCR_DTYPE_FP16, true, true>(tmap_h, tmap_h64, tmap_w, p, grid, s);
+  return pair ? launch_variant<HCR_DTYPE_FP16, true>(tmap_h, tmap_h64, tmap_w, p, grid, s)
+              : launch_variant<HCR_DTYPE_FP16, false>(tmap_h, tmap_h64, tmap_w, p, grid, s);
 }
 
 int project_pair_clusters(int dtype) {

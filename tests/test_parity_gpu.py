@@ -46,6 +46,10 @@ SMALL_CASES = [
     W("d8192", ModelShape("d8k", 1, 8192, 2, 2, 128), [300], [0]),
     W("block64", ModelShape("b64", 1, 256, 4, 4, 64), [333, 2], [65, 0], block_size=64,
       block_order="shuffled"),
+    # the CTA pairs' last tile: 128 rows (384 tokens) is a half tile, 129 rows
+    # (385) a full one
+    W("tail128", ModelShape("t128", 2, 256, 2, 2, 128), [100, 284], [0, 9]),
+    W("tail129", ModelShape("t129", 2, 256, 2, 2, 128), [100, 285], [0, 9]),
 ]
 
 
@@ -289,12 +293,14 @@ def test_variant_policy_decisions(cuda_device):
                                   shape.rope_theta, 16384, shape.dtype, shape.kv_bias), params)
     r7 = handle(LLAMA2_7B)
     h = r7.handle
-    want = {(64, 32): 1, (128, 32): 1, (256, 32): 2, (300, 32): 1, (500, 32): 2, (794, 32): 1,
+    # 300 and 794 tokens end in a half tail tile (<= 128 rows), so pairs pad no
+    # more than single CTAs there
+    want = {(64, 32): 1, (128, 32): 1, (256, 32): 2, (300, 32): 2, (500, 32): 2, (794, 32): 2,
             (4096, 32): 2, (4096, 4): 2, (16384, 32): 1, (629259, 8): 1}
     assert {k: B.hcr_project_variant(h, *k) for k in want} == want
     assert B.hcr_project_variant(h, 0, 32) == 0
     assert B.hcr_debug_set_variant(h, 2) == 0
-    assert B.hcr_project_variant(h, 300, 32) == 2
+    assert B.hcr_project_variant(h, 16384, 32) == 2
     assert B.hcr_debug_set_variant(h, 1) == 0
     assert B.hcr_project_variant(h, 4096, 32) == 1
     r13 = handle(LLAMA2_13B)

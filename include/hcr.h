@@ -440,13 +440,19 @@ hcr_status hcr_decode_hidden(hcr_handle* h, const hcr_codec_params* params, cons
  *     codes_host  [layer_end - layer_begin][n_tokens][d_model] int8
  *     scales_host [layer_end - layer_begin][n_tokens] float32
  * as hcr_encode_hidden writes them (with the same params).  Each group of
- * layers_per_chunk layers is copied (about half the bytes of the hidden
- * states), decoded on `stream` into a decode buffer, then restored.  The
- * caches are bit-identical to hcr_restore of hcr_decode_hidden's output.
- * staging (256-byte aligned) holds the decode buffer, align256(chunk * n_tokens
- * * d_model * 2) bytes, then the slots, each align256(chunk * n_tokens *
- * d_model) + align256(chunk * n_tokens * 4) bytes (up to 8 are used).  Other
- * arguments and behaviour are as in hcr_restore_streamed.
+ * layers is copied (about half the bytes of the hidden states) on the
+ * handle's copy stream, decoded into its staging slot on a second stream the
+ * handle owns (so later copies never wait for a decode), then restored on
+ * `stream`.  Groups grow 1, 2, 4 ... layers up to layers_per_chunk (the copy of
+ * the codes is about twice as fast as a restore, so small first groups start
+ * the restores early without stalling them later).  The caches are
+ * bit-identical to hcr_restore of hcr_decode_hidden's output.
+ * staging (256-byte aligned) holds the slots, each align256(chunk * n_tokens
+ * * d_model) + align256(chunk * n_tokens * 4) + align256(chunk * n_tokens *
+ * d_model * 2) bytes (codes, scales, decoded hidden states; up to 8 slots are
+ * used), chunk = min(layers_per_chunk, layer_end - layer_begin).  Codec
+ * parameters are checked as in hcr_decode_hidden before anything is
+ * enqueued.  Other arguments and behaviour are as in hcr_restore_streamed.
  */
 hcr_status hcr_restore_streamed_encoded(hcr_handle* h, const hcr_codec_params* params,
                                         const void* codes_host, const void* scales_host,

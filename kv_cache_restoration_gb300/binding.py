@@ -367,11 +367,12 @@ def hcr_decode_hidden(handle, params: hcr_codec_params, codes, scales, layer_beg
 
 
 def encoded_staging_bytes(n_tokens: int, d_model: int, layers_per_chunk: int, slots: int) -> int:
-    """Staging hcr_restore_streamed_encoded needs: the decode buffer plus `slots` slots."""
+    """Staging hcr_restore_streamed_encoded needs for `slots` slots of
+    `layers_per_chunk` layers (codes, scales and decoded hidden states each)."""
     def a(x):
         return (x + 255) // 256 * 256
     c = layers_per_chunk
-    return a(c * n_tokens * d_model * 2) + slots * (a(c * n_tokens * d_model) + a(c * n_tokens * 4))
+    return slots * (a(c * n_tokens * d_model) + a(c * n_tokens * 4) + a(c * n_tokens * d_model * 2))
 
 
 def hcr_restore_streamed_encoded(handle, params: hcr_codec_params, codes_host, scales_host,

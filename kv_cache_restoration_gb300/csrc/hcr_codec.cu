@@ -258,6 +258,8 @@ __global__ void __launch_bounds__(kCodecThreads) decode_kernel(const CodecParams
   }
 }
 
+}  // namespace
+
 hcr_status check_codec(const hcr_handle* h, const hcr_codec_params* cp, int32_t layer_begin,
                        int32_t layer_end, int32_t n_req, int32_t n_tokens,
                        const int32_t* cu_seqlens, bool* empty) {
@@ -284,6 +286,8 @@ hcr_status check_codec(const hcr_handle* h, const hcr_codec_params* cp, int32_t 
     return set_last_error(HCR_ERR_UNSUPPORTED, "codec supports bf16 and fp16 hidden states");
   return HCR_OK;
 }
+
+namespace {
 
 CodecParams make_params(const hcr_handle* h, const hcr_codec_params* cp, int32_t layer_begin,
                         int32_t n_req, int32_t n_tokens, const int32_t* cu_seqlens) {

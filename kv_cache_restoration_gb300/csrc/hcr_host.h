@@ -66,6 +66,12 @@ cudaError_t launch_kv_rows(const KvRowsParams& p, bool to_cache, int num_sms, cu
 // names `what` when the device cannot address it.
 hcr_status device_view(const Handle& H, void* ptr, const char* what, void** out);
 
+// Host checks of a codec call (hcr_encode_hidden / hcr_decode_hidden); sets
+// *empty for a call with no work.
+hcr_status check_codec(const hcr_handle* h, const hcr_codec_params* cp, int32_t layer_begin,
+                       int32_t layer_end, int32_t n_req, int32_t n_tokens,
+                       const int32_t* cu_seqlens, bool* empty);
+
 }  // namespace hcr
 
 struct hcr_handle {

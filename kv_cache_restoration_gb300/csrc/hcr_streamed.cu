@@ -30,8 +30,10 @@ namespace hcr {
 struct StreamedRes {
   std::mutex mutex;                 // one streamed restore enqueued at a time per handle
   cudaStream_t copy = nullptr;
+  cudaStream_t side = nullptr;      // work between a copy and its restore (the codec's decode)
   cudaEvent_t start = nullptr;
   cudaEvent_t copied[kMaxStagingSlots] = {};
+  cudaEvent_t landed[kMaxStagingSlots] = {};   // copy done, before the side work
   cudaEvent_t done[kMaxStagingSlots] = {};
 };
 
@@ -39,9 +41,11 @@ void release_streamed(Handle& H) {
   StreamedRes* r = H.streamed;
   if (!r) return;
   if (r->copy) cudaStreamDestroy(r->copy);
+  if (r->side) cudaStreamDestroy(r->side);
   if (r->start) cudaEventDestroy(r->start);
   for (int i = 0; i < kMaxStagingSlots; ++i) {
     if (r->copied[i]) cudaEventDestroy(r->copied[i]);
+    if (r->landed[i]) cudaEventDestroy(r->landed[i]);
     if (r->done[i]) cudaEventDestroy(r->done[i]);
   }
   delete r;
@@ -58,9 +62,11 @@ hcr_status ensure_resources(Handle& H, StreamedRes** out) {
     auto* r = new (std::nothrow) StreamedRes();
     if (!r) return set_last_error(HCR_ERR_OOM, "host allocation failed");
     cudaError_t e = cudaStreamCreateWithFlags(&r->copy, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&r->side, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->start, cudaEventDisableTiming);
     for (int i = 0; e == cudaSuccess && i < kMaxStagingSlots; ++i) {
       e = cudaEventCreateWithFlags(&r->copied[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->landed[i], cudaEventDisableTiming);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->done[i], cudaEventDisableTiming);
     }
     H.streamed = r;
@@ -84,7 +90,18 @@ struct Item {
 
 // Copies an item's host data into `dst` on `copy`: hidden states laid out
 // [nl][n_tokens][d_model], or K/V laid out [nl][2][n_tokens][d_kv].
-using CopyFn = std::function<cudaError_t(const Item& it, void* dst, cudaStream_t copy)>;
+using CopyFn = std::function<hcr_status(const Item& it, void* dst, cudaStream_t copy)>;
+
+// Optional GPU work between an item's copy and its processing (the codec's
+// decode), enqueued on the handle's side stream after the copy has landed, so
+// that the next copies do not queue behind it.
+using SideFn = std::function<hcr_status(const Item& it, void* dst, cudaStream_t side)>;
+
+hcr_status copy_status(cudaError_t e) {
+  if (e == cudaSuccess) return HCR_OK;
+  cudaGetLastError();
+  return set_last_error(HCR_ERR_CUDA, "host copy: %s", cudaGetErrorString(e));
+}
 
 // Enqueues an item's GPU work on the caller's stream once its copy has
 // landed in `src`: by default hcr_restore (hidden states) or hcr_load_kv
@@ -99,7 +116,7 @@ hcr_status run_pipeline(hcr_handle* h, const std::vector<Item>& items, size_t sl
                         void* v_cache, const hcr_cache_layout* layout, void* staging,
                         size_t staging_bytes, size_t workspace_need, void* workspace,
                         size_t workspace_bytes, void* stream, const CopyFn& copy_item,
-                        const ProcessFn* process = nullptr) {
+                        const ProcessFn* process = nullptr, const SideFn* side = nullptr) {
   NvtxRange range("hcr.streamed_pipeline");
   const hcr_model_dims& d = h->impl.dims;
   if (!layout) return set_last_error(HCR_ERR_INVALID_ARG, "layout is NULL");
@@ -142,9 +159,18 @@ hcr_status run_pipeline(hcr_handle* h, const std::vector<Item>& items, size_t sl
       return cuda_err(e, "stream wait");
     {
       NvtxRange copy_range(it.kv ? "hcr.copy_kv_group" : "hcr.copy_hidden_group");
-      if ((e = copy_item(it, dst, r->copy)) != cudaSuccess) return cuda_err(e, "host copy");
+      if ((st = copy_item(it, dst, r->copy)) != HCR_OK) return st;
     }
-    if ((e = cudaEventRecord(r->copied[slot], r->copy)) != cudaSuccess)
+    cudaStream_t ready = r->copy;   // where the item is ready for processing
+    if (side) {
+      if ((e = cudaEventRecord(r->landed[slot], r->copy)) != cudaSuccess)
+        return cuda_err(e, "event record");
+      if ((e = cudaStreamWaitEvent(r->side, r->landed[slot], 0)) != cudaSuccess)
+        return cuda_err(e, "stream wait");
+      if ((st = (*side)(it, dst, r->side)) != HCR_OK) return st;
+      ready = r->side;
+    }
+    if ((e = cudaEventRecord(r->copied[slot], ready)) != cudaSuccess)
       return cuda_err(e, "event record");
     if ((e = cudaStreamWaitEvent(s, r->copied[slot], 0)) != cudaSuccess)
       return cuda_err(e, "stream wait");
@@ -214,8 +240,9 @@ extern "C" hcr_status hcr_restore_streamed(
       h, layer_begin, layer_end, n_req, n_tokens, cu_seqlens, start_pos, block_table,
       max_blocks_per_req, k_cache, v_cache, layout, staging, staging_bytes, layers_per_chunk,
       workspace, workspace_bytes, stream, [&](const Item& it, void* dst, cudaStream_t copy) {
-        return cudaMemcpyAsync(dst, src + size_t(it.l0) * layer_bytes,
-                               size_t(it.nl) * layer_bytes, cudaMemcpyHostToDevice, copy);
+        return copy_status(cudaMemcpyAsync(dst, src + size_t(it.l0) * layer_bytes,
+                                           size_t(it.nl) * layer_bytes, cudaMemcpyHostToDevice,
+                                           copy));
       });
 }
 
@@ -315,9 +342,9 @@ extern "C" hcr_status hcr_restore_streamed_chunks(
                                     layer_in_chunk, run.width, size_t(nl),
                                     cudaMemcpyHostToDevice, copy);
           }
-          if (e != cudaSuccess) return e;
+          if (e != cudaSuccess) return copy_status(e);
         }
-        return cudaSuccess;
+        return HCR_OK;
       });
 }
 
@@ -371,10 +398,12 @@ extern "C" hcr_status hcr_restore_streamed_split(
       hcr_workspace_bytes(h, n_tokens, std::max(ch, 1)), workspace, workspace_bytes, stream,
       [&](const Item& it, void* dst, cudaStream_t copy) {
         if (it.kv)
-          return cudaMemcpyAsync(dst, kv + size_t(it.l0 - n_hid) * kv_layer,
-                                 size_t(it.nl) * kv_layer, cudaMemcpyHostToDevice, copy);
-        return cudaMemcpyAsync(dst, hid + size_t(it.l0) * hid_layer, size_t(it.nl) * hid_layer,
-                               cudaMemcpyHostToDevice, copy);
+          return copy_status(cudaMemcpyAsync(dst, kv + size_t(it.l0 - n_hid) * kv_layer,
+                                             size_t(it.nl) * kv_layer, cudaMemcpyHostToDevice,
+                                             copy));
+        return copy_status(cudaMemcpyAsync(dst, hid + size_t(it.l0) * hid_layer,
+                                           size_t(it.nl) * hid_layer, cudaMemcpyHostToDevice,
+                                           copy));
       });
 }
 
@@ -394,6 +423,10 @@ extern "C" hcr_status hcr_restore_streamed_encoded(
   if (n_tokens == 0 || layer_end == layer_begin) return HCR_OK;
   if (!params || !codes_host || !scales_host)
     return set_last_error(HCR_ERR_INVALID_ARG, "params, codes_host and scales_host are needed");
+  bool empty = false;
+  hcr_status st = check_codec(h, params, layer_begin, layer_end, n_req, n_tokens, cu_seqlens,
+                              &empty);
+  if (st != HCR_OK || empty) return st;
   if (layers_per_chunk < 1)
     return set_last_error(HCR_ERR_INVALID_ARG, "layers_per_chunk must be >= 1");
   if (!staging || reinterpret_cast<uintptr_t>(staging) % 256)
@@ -401,43 +434,46 @@ extern "C" hcr_status hcr_restore_streamed_encoded(
   const int32_t n_layers = layer_end - layer_begin;
   const int32_t chunk = std::min(layers_per_chunk, n_layers);
   const size_t T = size_t(n_tokens), dm = size_t(d.d_model);
-  // staging: [decoded hidden states of one group][slot 0: codes | scales][slot 1] ...
-  const size_t decoded_bytes = align_up(size_t(chunk) * T * dm * 2, 256);
+  // a slot: [codes][scales][decoded hidden states], each 256-byte aligned
   const size_t codes_bytes = align_up(size_t(chunk) * T * dm, 256);
-  const size_t slot_bytes = codes_bytes + align_up(size_t(chunk) * T * 4, 256);
-  if (staging_bytes < decoded_bytes + slot_bytes)
-    return set_last_error(HCR_ERR_WORKSPACE, "staging has %zu bytes; the decode buffer and "
-                          "one slot need %zu", staging_bytes, decoded_bytes + slot_bytes);
-  void* decoded = staging;
+  const size_t scales_bytes = align_up(size_t(chunk) * T * 4, 256);
+  const size_t slot_bytes = codes_bytes + scales_bytes + align_up(size_t(chunk) * T * dm * 2, 256);
+  // The codes are half the hidden states' bytes, so a group's copy takes
+  // about half as long as its restore: groups of 1, 2, 4 ... layers up to
+  // `chunk` start the first restore early without the restores ever waiting
+  // on a copy.
   std::vector<Item> items;
-  for (int32_t l0 = 0; l0 < n_layers; l0 += chunk)
-    items.push_back({false, l0, std::min(chunk, n_layers - l0)});
+  for (int32_t l0 = 0, nl = 1; l0 < n_layers; l0 += nl, nl = std::min(2 * nl, chunk))
+    items.push_back({false, l0, std::min(nl, n_layers - l0)});
   const uint8_t* codes = static_cast<const uint8_t*>(codes_host);
   const uint8_t* scales = static_cast<const uint8_t*>(scales_host);
-  // The decode of group i+1 follows the restore of group i on the caller's
-  // stream, so one decode buffer serves every group.
-  const ProcessFn decode_then_restore = [&](const Item& it, void* src, int32_t lb, void* kc,
-                                            void* vc) {
-    const uint8_t* slot = static_cast<const uint8_t*>(src);
-    hcr_status st = hcr_decode_hidden(h, params, slot, slot + codes_bytes, lb, lb + it.nl,
-                                      n_req, n_tokens, cu_seqlens, decoded, stream);
-    if (st != HCR_OK) return st;
-    return hcr_restore(h, decoded, lb, lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos,
-                       block_table, max_blocks_per_req, kc, vc, layout, workspace,
-                       workspace_bytes, stream);
+  // The decode runs on the side stream once the group's codes have landed, so
+  // the copies of the next groups go on meanwhile; the restore reads the
+  // slot's decoded part.
+  const SideFn decode = [&](const Item& it, void* dst, cudaStream_t side) {
+    uint8_t* slot = static_cast<uint8_t*>(dst);
+    const int32_t lb = layer_begin + it.l0;
+    return hcr_decode_hidden(h, params, slot, slot + codes_bytes, lb, lb + it.nl, n_req,
+                             n_tokens, cu_seqlens, slot + codes_bytes + scales_bytes, side);
+  };
+  const ProcessFn restore_decoded = [&](const Item& it, void* src, int32_t lb, void* kc,
+                                        void* vc) {
+    return hcr_restore(h, static_cast<uint8_t*>(src) + codes_bytes + scales_bytes, lb,
+                       lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos, block_table,
+                       max_blocks_per_req, kc, vc, layout, workspace, workspace_bytes, stream);
   };
   return run_pipeline(
       h, items, slot_bytes, layer_begin, n_req, n_tokens, cu_seqlens, start_pos, block_table,
-      max_blocks_per_req, k_cache, v_cache, layout, static_cast<uint8_t*>(staging) + decoded_bytes,
-      staging_bytes - decoded_bytes, hcr_workspace_bytes(h, n_tokens, chunk), workspace,
-      workspace_bytes, stream,
+      max_blocks_per_req, k_cache, v_cache, layout, staging, staging_bytes,
+      hcr_workspace_bytes(h, n_tokens, chunk), workspace, workspace_bytes, stream,
       [&](const Item& it, void* dst, cudaStream_t copy) {
         uint8_t* slot = static_cast<uint8_t*>(dst);
         cudaError_t e = cudaMemcpyAsync(slot, codes + size_t(it.l0) * T * dm,
                                         size_t(it.nl) * T * dm, cudaMemcpyHostToDevice, copy);
-        if (e != cudaSuccess) return e;
-        return cudaMemcpyAsync(slot + codes_bytes, scales + size_t(it.l0) * T * 4,
-                               size_t(it.nl) * T * 4, cudaMemcpyHostToDevice, copy);
+        if (e == cudaSuccess)
+          e = cudaMemcpyAsync(slot + codes_bytes, scales + size_t(it.l0) * T * 4,
+                              size_t(it.nl) * T * 4, cudaMemcpyHostToDevice, copy);
+        return copy_status(e);
       },
-      &decode_then_restore);
+      &restore_decoded, &decode);
 }

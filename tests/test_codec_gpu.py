@@ -9,6 +9,7 @@ import torch
 from oracle import codec as K
 from tests import harness as Hn
 from workloads import configs as C
+from workloads import generate as G
 from workloads.configs import ModelShape, Workload
 
 pytestmark = pytest.mark.gpu
@@ -194,3 +195,26 @@ def test_streamed_encoded_rejects_small_staging(cuda_device):
         B.hcr_cache_layout(lay.num_blocks, lay.block_size, 0), staging, need - 256, 2, ws,
         ws.numel(), torch.cuda.current_stream(), check=False)
     assert st == B.HCR_ERR_WORKSPACE
+
+
+def test_streamed_encoded_rejects_bad_params_before_enqueueing(cuda_device):
+    from kv_cache_restoration_gb300 import binding as B
+    case = Hn.make_case(W, cuda_device)
+    lay = case.layout
+    T, d = W.n_tokens, W.shape.d_model
+    need = B.encoded_staging_bytes(T, d, 2, 2)
+    staging = torch.full((need,), 0x5A, dtype=torch.uint8, device=cuda_device)
+    ws = torch.empty(B.hcr_workspace_bytes(case.restorer.handle, T, 2) + 256, dtype=torch.uint8,
+                     device=cuda_device)
+    codes = torch.ones((6, T, d), dtype=torch.int8).pin_memory()
+    scales = torch.ones((6, T), dtype=torch.float32).pin_memory()
+    for p in (B.codec_params((0.5, 0.0, 1.5)), B.codec_params(group_tokens=0)):
+        st = B.hcr_restore_streamed_encoded(
+            case.restorer.handle, p, codes, scales, 0, 6, int(case.start.numel()), T, case.cu,
+            case.start, case.table, lay.max_blocks, case.k_cache, case.v_cache,
+            B.hcr_cache_layout(lay.num_blocks, lay.block_size, 0), staging, need, 2, ws,
+            ws.numel(), torch.cuda.current_stream(), check=False)
+        assert st == B.HCR_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert bool((staging == 0x5A).all())          # no copy was enqueued
+    assert bool((case.k_cache.view(torch.int16) == G.SENTINEL_BITS).all())

@@ -86,3 +86,58 @@ def test_null_handle_calls(B):
                        check=False)
     assert st == B.HCR_ERR_INVALID_ARG
     assert B.hcr_check_device_error(None)[0] == B.HCR_ERR_INVALID_ARG
+
+
+C_CONSUMER = r"""
+/* A plain C11 caller of the boundary: no C++, no CUDA headers. */
+#include <stdio.h>
+#include <string.h>
+#include "hcr.h"
+
+static int expect(int cond, const char* what) {
+  if (!cond) fprintf(stderr, "failed: %s (last error: %s)\n", what, hcr_last_error());
+  return cond ? 0 : 1;
+}
+
+int main(void) {
+  int bad = 0;
+  hcr_handle* h = NULL;
+  hcr_model_dims d;
+  memset(&d, 0, sizeof d);
+  d.n_layers = 2; d.d_model = 256; d.n_heads = 4; d.n_kv_heads = 4; d.head_dim = 96;
+  d.norm = HCR_NORM_RMS; d.norm_eps = 1e-5f; d.rope = HCR_ROPE_ROTATE_HALF;
+  d.rope_theta = 10000.f; d.max_position = 128; d.dtype = HCR_DTYPE_BF16;
+  bad += expect(hcr_create(NULL, NULL, NULL, NULL, NULL, NULL, NULL, &h) ==
+                HCR_ERR_INVALID_ARG && h == NULL, "create without dims");
+  bad += expect(hcr_create(&d, NULL, NULL, NULL, NULL, NULL, NULL, &h) != HCR_OK && h == NULL,
+                "create with head_dim 96");
+  bad += expect(strlen(hcr_last_error()) > 0, "last error names the failure");
+  bad += expect(strcmp(hcr_status_string(HCR_OK), "HCR_OK") == 0, "status string");
+  bad += expect(hcr_restore(NULL, NULL, 0, 1, 1, 1, NULL, NULL, NULL, 1, NULL, NULL, NULL, NULL,
+                            0, NULL) == HCR_ERR_INVALID_ARG, "restore without a handle");
+  hcr_destroy(NULL);
+  if (!bad) printf("c consumer ok\n");
+  return bad;
+}
+"""
+
+
+def test_plain_c_consumer_compiles_links_and_runs(B, tmp_path):
+    """include/hcr.h is a C header: a C11 program (gcc -std=c11 -pedantic,
+    warnings as errors) includes it, links libhcr.so and calls the host-side
+    paths that need no GPU."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src, exe = tmp_path / "consumer.c", tmp_path / "consumer"
+    src.write_text(C_CONSUMER)
+    libdir = os.path.dirname(B.LIB)
+    cmd = [gcc, "-std=c11", "-pedantic", "-Wall", "-Wextra", "-Werror",
+           "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+           "-L", libdir, "-l:" + os.path.basename(B.LIB), "-Wl,-rpath," + libdir]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and "c consumer ok" in r.stdout, (r.stdout, r.stderr)

@@ -298,18 +298,20 @@ def gpu_arm(args, rank, world, local_rank):
     # layer-pipelined entry point (copies of later layers overlap the restore of
     # earlier ones); the host reads the 4-byte status word each step.
     from kv_cache_restoration_gb300 import binding as B
-    hidden_host = case.hidden.cpu().pin_memory()
+    # the end-to-end leg needs every layer's hidden states in host memory and
+    # one restore over them; a windowed workload has no such leg (and pins no
+    # host copy of its window)
+    e2e_steps = min(args.steps, args.e2e_steps) if nw == 1 else 0
+    hidden_host = case.hidden.cpu().pin_memory() if e2e_steps > 0 else None
     meta_host = [t.cpu().pin_memory() for t in (case.cu, case.start, case.table)]
     meta_dev = [case.cu, case.start, case.table]
-    h2d = hidden_host.numel() * hidden_host.element_size() + sum(
+    h2d = (hidden_host.numel() * hidden_host.element_size() if e2e_steps > 0 else 0) + sum(
         m.numel() * m.element_size() for m in meta_host)
     chunk = max(1, min(args.e2e_chunk, L))
     chunk_bytes = chunk * T * s.d_model * 2
-    staging = torch.empty(args.e2e_slots * chunk_bytes, dtype=torch.uint8, device=device)
+    staging = torch.empty(args.e2e_slots * chunk_bytes if e2e_steps > 0 else 256,
+                          dtype=torch.uint8, device=device)
     layout = B.hcr_cache_layout(lay.num_blocks, lay.block_size, 0)
-    # the end-to-end leg needs every layer's hidden states in host memory and
-    # one restore over them; a windowed workload has no such leg
-    e2e_steps = min(args.steps, args.e2e_steps) if nw == 1 else 0
     src = None
     if args.e2e_source == "chunks" and e2e_steps > 0:
         # The saved form: 64-token chunks [chunk][layer][row][d] in pinned host

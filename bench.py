@@ -16,6 +16,7 @@ region is bracketed by barriers and the slowest rank's time is reported.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -382,6 +383,11 @@ def gpu_arm(args, rank, world, local_rank):
     t0 = time.perf_counter()
     step_s = []
     ew = args.e2e_warmup
+    # Each step waits on the host, so a pause of this process would land in
+    # the step's time: collect once here and keep the cyclic collector off
+    # while the leg runs.
+    gc.collect()
+    gc.disable()
     for i in range(ew + e2e_steps if e2e_steps > 0 else 0):
         if i == ew:
             torch.cuda.synchronize(device)
@@ -416,6 +422,7 @@ def gpu_arm(args, rank, world, local_rank):
         if i >= ew:
             step_s.append(time.perf_counter() - ts)
     e2e_s = (time.perf_counter() - t0) / e2e_steps if e2e_steps > 0 else float("nan")
+    gc.enable()
     # context: one plain copy of all hidden states, host to device
     h2d_gbs = None
     if e2e_steps > 0:

@@ -876,8 +876,12 @@ def main():
     if t_tensor >= t_hbm:
         # The denominator matches the regime the timed region ran in: the
         # sustained bf16 figure was measured as a seconds-long loop under the
-        # power cap, the burst one without it.  The clock samples say which.
-        capped = "sw_power_cap" in (res["clocks"].get("reasons") or [])
+        # power cap, the burst one without it.  The clock samples say which: the
+        # cap active and the median SM clock held below 95% of its maximum (a
+        # short run can touch the cap while its clock stays near the top).
+        clk = res["clocks"]
+        capped = ("sw_power_cap" in (clk.get("reasons") or []) and clk.get("sm_mhz")
+                  and clk.get("sm_max_mhz") and clk["sm_mhz"] < 0.95 * clk["sm_max_mhz"])
         achieved = flops / proj_s / 1e12
         roofline = {"bound": "tensor", "achieved": achieved,
                     "peak": peaks["bf16_tflops_sustained" if capped else "bf16_tflops"],

@@ -8,9 +8,9 @@
 //     block or position is out of range get slot -1 (never written) and set
 //     a device error bit.
 //   * norm statistics -- one warp per (layer, token) row of the saved hidden
-//     states: RMSNorm rstd = 1/sqrt(mean(h^2) + eps); LayerNorm mean and
-//     rstd = 1/sqrt(biased var + eps), accumulated around the row's first
-//     element for conditioning.  The hidden states are the layer inputs the
+//     states: RMSNorm rstd = 1/sqrt(mean(h^2) + eps); LayerNorm mean, then
+//     rstd = 1/sqrt(biased var + eps) from a second pass of squared
+//     deviations from that mean.  The hidden states are the layer inputs the
 //     HCache episode ("Fast State Restoration for Evicted LLM KV Caches",
 //     cue 14) restores from; applying the input norm is this library's
 //     reading of its K = W_k H shorthand for pre-norm models.
@@ -112,8 +112,31 @@ __device__ void row_stats(const PrepareParams& p, int64_t row, int lane) {
   const uint16_t* h = reinterpret_cast<const uint16_t*>(p.hidden) + row * int64_t(d);
   const uint4* hv = reinterpret_cast<const uint4*>(h);
   const int nvec = d >> 3;
-  const float shift = p.layer_norm ? to_float<DT>(__ldg(h)) : 0.f;
-  float s1 = 0.f, s2 = 0.f;
+  const float inv_d = 1.0f / float(d);
+  if (!p.layer_norm) {
+    float s2 = 0.f;
+#pragma unroll 4
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 q = __ldg(hv + v);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = to_float2<DT>(w[k]);
+        s2 = fmaf(f.x, f.x, s2);
+        s2 = fmaf(f.y, f.y, s2);
+      }
+    }
+    s2 = warp_sum(s2);
+    if (lane == 0) p.rstd[row] = 1.0f / sqrtf(s2 * inv_d + p.eps);
+    return;
+  }
+  // LayerNorm in two passes over the row: the mean (summed around the row's
+  // first element, which keeps the partial sums small when |mean| >> spread),
+  // then the sum of squared deviations from that mean.  The second pass reads
+  // the row again from L1/L2.  A one-pass sum(x^2) - mean^2 cancels when
+  // |mean| or an outlier channel is large against the spread.
+  const float shift = to_float<DT>(__ldg(h));
+  float s1 = 0.f;
 #pragma unroll 4
   for (int v = lane; v < nvec; v += 32) {
     const uint4 q = __ldg(hv + v);
@@ -121,24 +144,28 @@ __device__ void row_stats(const PrepareParams& p, int64_t row, int lane) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float2 f = to_float2<DT>(w[k]);
-      const float x0 = f.x - shift, x1 = f.y - shift;
-      s1 += x0 + x1;
+      s1 += (f.x - shift) + (f.y - shift);
+    }
+  }
+  s1 = warp_sum(s1);
+  const float mean = shift + s1 * inv_d;
+  float s2 = 0.f;
+#pragma unroll 4
+  for (int v = lane; v < nvec; v += 32) {
+    const uint4 q = __ldg(hv + v);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = to_float2<DT>(w[k]);
+      const float x0 = f.x - mean, x1 = f.y - mean;
       s2 = fmaf(x0, x0, s2);
       s2 = fmaf(x1, x1, s2);
     }
   }
-  s1 = warp_sum(s1);
   s2 = warp_sum(s2);
   if (lane == 0) {
-    const float inv_d = 1.0f / float(d);
-    if (p.layer_norm) {
-      const float m1 = s1 * inv_d;
-      const float var = fmaxf(s2 * inv_d - m1 * m1, 0.f);
-      p.mean[row] = shift + m1;
-      p.rstd[row] = 1.0f / sqrtf(var + p.eps);
-    } else {
-      p.rstd[row] = 1.0f / sqrtf(s2 * inv_d + p.eps);
-    }
+    p.mean[row] = mean;
+    p.rstd[row] = 1.0f / sqrtf(s2 * inv_d + p.eps);
   }
 }
 

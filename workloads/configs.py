@@ -54,6 +54,14 @@ class Workload:
     seed: int = 0
     max_position: int = 0             # RoPE table size; 0 -> derived
     description: str = ""
+    # Hidden-state distribution.  Default: every element ~ N(0,1).  With
+    # hidden_means, each token row gets a mean drawn (seeded, uniformly) from
+    # this set and added to its N(0,1) draw; outlier_channels are scaled by
+    # outlier_scale before the mean is added.  Large row means and a few
+    # large channels are what real LayerNorm inputs (OPT) carry.
+    hidden_means: Tuple[float, ...] = ()
+    outlier_channels: Tuple[int, ...] = ()
+    outlier_scale: float = 1.0
 
     @property
     def n_req(self) -> int:

@@ -28,7 +28,7 @@ from .configs import ModelShape, Workload
 TORCH_DTYPE = {"bf16": torch.bfloat16, "fp16": torch.float16}
 
 _TAGS = {"hidden": 1, "gamma": 2, "beta": 3, "w_k": 4, "w_v": 5, "b_k": 6, "b_v": 7,
-         "blocks": 8}
+         "blocks": 8, "row_mean": 9}
 
 _MASK64 = (1 << 64) - 1
 
@@ -49,11 +49,13 @@ def stream_seed(seed: int, tag: str, layer: int = 0, chunk: int = 0) -> int:
 
 
 def normal(shape, mean: float, std: float, seed: int, device, dtype: torch.dtype,
-           chunk_rows: int = 0) -> torch.Tensor:
+           chunk_rows: int = 0, post=None) -> torch.Tensor:
     """N(mean, std^2) drawn in fp32 then rounded once to `dtype`.
 
     With chunk_rows > 0 the leading dimension is drawn in chunks of that many
-    rows, each from its own stream, to bound the fp32 temporary.
+    rows, each from its own stream, to bound the fp32 temporary.  `post`, if
+    given, is called as post(x, r0, r1) on each fp32 chunk (rows r0..r1-1)
+    before the rounding and may change it in place.
     """
     device = torch.device(device)
     out = torch.empty(shape, dtype=dtype, device=device)
@@ -69,6 +71,8 @@ def normal(shape, mean: float, std: float, seed: int, device, dtype: torch.dtype
             x.mul_(std)
         if mean != 0.0:
             x.add_(mean)
+        if post is not None:
+            post(x, r0, r1)
         out[r0:r1] = x.to(dtype)
     return out
 
@@ -98,12 +102,34 @@ def layer_params(shape: ModelShape, layer: int, seed: int, device="cpu") -> Laye
     return LayerParams(gamma, beta, w_k, w_v, b_k, b_v)
 
 
+def hidden_row_means(w: Workload, layer: int) -> Optional[np.ndarray]:
+    """The mean added to each token row of layer `layer`'s hidden states (a
+    seeded uniform choice from w.hidden_means), or None for zero-mean rows."""
+    if not w.hidden_means:
+        return None
+    rng = np.random.Generator(np.random.PCG64(stream_seed(w.seed, "row_mean", layer)))
+    pick = rng.integers(0, len(w.hidden_means), size=w.n_tokens)
+    return np.asarray(w.hidden_means, np.float32)[pick]
+
+
 def hidden_states(w: Workload, layer: int, device="cpu", out: Optional[torch.Tensor] = None,
                   chunk_rows: int = 65536) -> torch.Tensor:
     """Saved layer input H_l [T, d] for the workload's concatenated tokens."""
     dt = TORCH_DTYPE[w.shape.dtype]
+    post = None
+    if w.hidden_means or w.outlier_channels:
+        means = hidden_row_means(w, layer)
+        row_mean = None if means is None else torch.as_tensor(means, device=device)
+        cols = torch.as_tensor(list(w.outlier_channels), dtype=torch.long, device=device)
+
+        def post(x, r0, r1):
+            if len(w.outlier_channels):
+                x[:, cols] *= w.outlier_scale
+            if row_mean is not None:
+                x.add_(row_mean[r0:r1, None])
     h = normal((w.n_tokens, w.shape.d_model), 0.0, 1.0,
-               stream_seed(w.seed, "hidden", layer), device, dt, chunk_rows=chunk_rows)
+               stream_seed(w.seed, "hidden", layer), device, dt, chunk_rows=chunk_rows,
+               post=post)
     if out is not None:
         out.copy_(h)
         return out

@@ -148,6 +148,42 @@ def whole_job_tokens_per_s(world: int, tokens_per_rank: int, t_step_max: float) 
     return world * tokens_per_rank / t_step_max
 
 
+def layer_windows(args, w):
+    """Layers per restore call and the calls of one step.  A workload whose
+    hidden states and caches for all layers exceed HBM (the ragged batch)
+    restores in windows of layers: one window of buffers is allocated and
+    every window's restore reads it, back to back, so the step is the whole
+    restore at the GPU's sustained load."""
+    L = w.shape.n_layers
+    win = args.window_layers if args.window_layers >= 0 else (8 if w.name == "ragged-7b" else 0)
+    win = min(win, L) if win > 0 else L
+    return win, [(lb, min(lb + win, L)) for lb in range(0, L, win)]
+
+
+def workload_description(w):
+    s = w.shape
+    return (f"{w.name}: {s.n_layers} layers, d={s.d_model}, {s.n_kv_heads}x{s.head_dim}"
+            f" KV heads, {w.n_req} request(s), {w.n_tokens} tokens, {s.norm}, "
+            f"{'RoPE' if s.rope else 'no RoPE'}, block {w.block_size} "
+            f"({w.block_order}), {s.dtype}")
+
+
+def line_config(args, w, world):
+    """The `config` object of a bench line; both arms print the same one."""
+    flops, hid_b, w_b, kv_b = algorithmic_work(w.shape, w.n_tokens, w.shape.n_layers)
+    win, windows = layer_windows(args, w)
+    cfg = {"workload": workload_description(w),
+           "parallelism": "replicas" if world > 1 else "single GPU",
+           "l2": f"inputs larger than L2 ({(hid_b + w_b + kv_b) / 1e9:.2f} GB "
+                 "moved per step vs 129 MB L2); no flush"}
+    if len(windows) > 1:
+        cfg["layer_windows"] = (f"{len(windows)} windows of {win} layers restored back to back "
+                                "per step; hidden states and caches of all layers exceed HBM, "
+                                "so one window of buffers is allocated and every window reads "
+                                "and writes it")
+    return cfg
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_child(args):
     """Runs in a fresh interpreter: time the oracle on a bounded sample of the
@@ -177,17 +213,21 @@ def oracle_child(args):
     for _ in range(args.oracle_warmup):
         R.restore_layer(h, lw, pos, spec)
     times = []
+    # seconds > 0: repeat until that much time has passed (at most max_reps);
+    # seconds <= 0: exactly max_reps timed reps
     t_end = time.perf_counter() + args.oracle_seconds
     while True:
         t0 = time.perf_counter()
         R.restore_layer(h, lw, pos, spec)
         times.append(time.perf_counter() - t0)
-        if time.perf_counter() >= t_end or len(times) >= args.oracle_max_reps:
+        if len(times) >= args.oracle_max_reps:
+            break
+        if args.oracle_seconds > 0 and time.perf_counter() >= t_end:
             break
     t = statistics.mean(times)
     # full-model tokens/s: one layer of `rows` tokens is 1/L of restoring them
     print(json.dumps({"seconds_per_layer_sample": t, "rows": rows, "reps": len(times),
-                      "value": rows / (t * s.n_layers)}))
+                      "seconds_total": sum(times), "value": rows / (t * s.n_layers)}))
 
 
 def run_oracle(workload: str, rows: int, seconds: float, max_reps: int, warmup: int = 0,
@@ -231,13 +271,7 @@ def gpu_arm(args, rank, world, local_rank):
     if args.layers:
         w = C.with_layers(w, args.layers)
     s = w.shape
-    # A workload whose hidden states and caches for all layers exceed HBM (the
-    # ragged batch) restores in windows of layers: one window of buffers is
-    # allocated and every window's restore reads it, back to back, so the step
-    # is the whole restore at the GPU's sustained load.
-    win = args.window_layers if args.window_layers >= 0 else (8 if w.name == "ragged-7b" else 0)
-    win = min(win, s.n_layers) if win > 0 else s.n_layers
-    windows = [(lb, min(lb + win, s.n_layers)) for lb in range(0, s.n_layers, win)]
+    win, windows = layer_windows(args, w)
     case = G.device_inputs(w, device, 0, win, gen_device=device)
     r = Restorer(make_dims(s.n_layers, s.d_model, s.n_heads, s.n_kv_heads, s.head_dim, s.norm,
                            s.norm_eps, s.rope, s.rope_theta, w.rope_positions, s.dtype,
@@ -449,6 +483,122 @@ def gpu_arm(args, rank, world, local_rank):
                 split=split_plan, torch_ctx=torch_ctx,
                 variant=B.hcr_project_variant(r.handle, T, windows[0][1] - windows[0][0]),
                 e2e_median_s=e2e_med, e2e_p90_s=e2e_p90, e2e_max_s=e2e_max)
+
+
+# The benchmark spec's targets beside the headline: each workload restored through
+# the same two stages, timed the same way (CUDA events on the launching stream,
+# clocks sampled during the timed region).  Steps per workload keep each timed
+# region at a few tenths of a second.  target: the fraction of the roofline's
+# peak the restore should reach (None: reported only).
+TARGETS = [
+    # name, timed steps, warm-up steps, target fraction
+    ("llama2-13b", 10, 3, 0.60),
+    ("opt-30b", 8, 3, None),
+    ("llama2-7b-T64", 1000, 20, 0.70),
+    ("llama2-7b-T300", 600, 20, 0.70),
+    ("llama2-7b-T794", 300, 10, 0.60),
+]
+
+
+def roofline_of(w, proj_s, t_step, peaks, peak_kind, clocks):
+    """Roofline record of one restore: the project kernel's achieved rate
+    against the peak of the bound (tensor or HBM), as in the headline line."""
+    s = w.shape
+    flops, hid_b, w_b, kv_b = algorithmic_work(s, w.n_tokens, s.n_layers)
+    t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = (hid_b + w_b + kv_b) / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        capped = ("sw_power_cap" in (clocks.get("reasons") or []) and clocks.get("sm_mhz")
+                  and clocks.get("sm_max_mhz") and clocks["sm_mhz"] < 0.95 * clocks["sm_max_mhz"])
+        achieved = flops / proj_s / 1e12
+        rec = {"bound": "tensor", "achieved": achieved,
+               "peak": peaks["bf16_tflops_sustained" if capped else "bf16_tflops"],
+               "unit": "TFLOP/s",
+               "peak_source": (f"{peak_kind} bf16 sustained (the timed region ran under the "
+                               "power cap)" if capped else f"{peak_kind} bf16 burst"),
+               "frac_of_burst": achieved / peaks["bf16_tflops"],
+               "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
+    else:
+        rec = {"bound": "hbm", "achieved": (hid_b + w_b + kv_b) / proj_s / 1e9,
+               "peak": peaks["hbm_gbs"], "unit": "GB/s",
+               "peak_source": f"{peak_kind} HBM copy bandwidth"}
+    rec["frac"] = rec["achieved"] / rec["peak"]
+    rec["step_roofline_frac"] = max(t_tensor, t_hbm) / t_step
+    return rec
+
+
+def targets_leg(device, peaks, peak_kind, only=None):
+    """Times every TARGETS workload on this GPU; returns {name: record}."""
+    import torch
+
+    from kv_cache_restoration_gb300 import Restorer, make_dims
+    from kv_cache_restoration_gb300 import binding as B
+    from workloads import configs as C
+    from workloads import generate as G
+
+    out = {}
+    stream = torch.cuda.current_stream(device)
+    for name, steps, warmup, target in TARGETS:
+        if only and name not in only:
+            continue
+        w = C.get(name)
+        s = w.shape
+        L, T = s.n_layers, w.n_tokens
+        case = G.device_inputs(w, device, gen_device=device)
+        r = Restorer(make_dims(L, s.d_model, s.n_heads, s.n_kv_heads, s.head_dim, s.norm,
+                               s.norm_eps, s.rope, s.rope_theta, w.rope_positions, s.dtype,
+                               s.kv_bias), case.params)
+        case.params = None
+        lay = case.layout
+        ws = r.workspace(T, L, device)
+
+        def stage(name_):
+            r.restore(case.hidden, 0, L, case.cu, case.start, case.table, case.k_cache,
+                      case.v_cache, lay.num_blocks, lay.block_size, stream=stream, workspace=ws,
+                      stage=name_)
+
+        for _ in range(warmup):
+            stage("prepare")
+            stage("project")
+        st, flags = r.check(stream)
+        if st != 0:
+            raise RuntimeError(f"{name}: device error {st} flags {flags:#x}")
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        gpu_id = getattr(torch.cuda.get_device_properties(device), "uuid", None)
+        gpu_id = f"GPU-{gpu_id}" if gpu_id is not None else str(device.index or 0)
+        torch.cuda.synchronize(device)
+        with ClockSampler(str(gpu_id)) as clk:
+            torch.cuda.synchronize(device)
+            for e in ev:
+                e[0].record(stream)
+                stage("prepare")
+                e[1].record(stream)
+                stage("project")
+                e[2].record(stream)
+            torch.cuda.synchronize(device)
+        st, flags = r.check(stream)
+        if st != 0:
+            raise RuntimeError(f"{name}: device error {st} flags {flags:#x}")
+        total_s = ev[0][0].elapsed_time(ev[-1][2]) / 1e3
+        t_step = total_s / steps
+        prep_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        proj_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+        clocks = clk.summary()
+        roof = roofline_of(w, proj_ms / 1e3, t_step, peaks, peak_kind, clocks)
+        out[name] = {
+            "workload": workload_description(w),
+            "steps": steps, "warmup": warmup, "timed_s": total_s,
+            "ms_per_step": t_step * 1e3, "tokens_per_s": T / t_step,
+            "stage_ms": {"prepare": prep_ms, "project": proj_ms},
+            "project_variant": {1: "single CTAs", 2: "CTA pairs"}.get(
+                B.hcr_project_variant(r.handle, T, L), "?"),
+            "roofline": roof, "clocks": clocks,
+            "target": target, "met": None if target is None else bool(roof["frac"] >= target),
+        }
+        del case, r, ws
+        gc.collect()
+        torch.cuda.empty_cache()
+    return out
 
 
 def torch_composite_ms(w, case, device, stream, reps: int = 3):
@@ -793,6 +943,10 @@ def main():
                     help="project kernel tiles: 0 automatic, 1 single CTAs, 2 CTA pairs")
     ap.add_argument("--layers", type=int, default=0,
                     help="cut the model to its first N layers (small profiling cases)")
+    ap.add_argument("--targets", default="auto",
+                    help="auto: time the north-star target workloads (13B, OPT-30B, short "
+                         "7B restores) after the headline, on one GPU, for the default "
+                         "workload; off; or a comma-separated subset of their names")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--torch-context", type=int, default=1,
                     help="1: also time the restore written as PyTorch ops (context only)")
@@ -824,31 +978,38 @@ def main():
     if args.layers:
         w = C.with_layers(w, args.layers)
     s = w.shape
-    workload_desc = (f"{w.name}: {s.n_layers} layers, d={s.d_model}, {s.n_kv_heads}x{s.head_dim}"
-                     f" KV heads, {w.n_req} request(s), {w.n_tokens} tokens, {s.norm}, "
-                     f"{'RoPE' if s.rope else 'no RoPE'}, block {w.block_size} "
-                     f"({w.block_order}), {s.dtype}")
+    world_cfg = int(os.environ.get("WORLD_SIZE", "1"))
+    config = line_config(args, w, world_cfg)
     flops, hid_b, w_b, kv_b = algorithmic_work(s, w.n_tokens, s.n_layers)
     peaks, peak_kind = load_peaks()
 
     if args.impl == "reference":
         if rank != 0:
             return
-        # size each step's sample so warmup+steps end within ~2 minutes
+        # Each step is one timed rep of the oracle on a sample of the workload:
+        # one layer of `rows` tokens, sized from a probe so that the warm-up and
+        # timed reps together take about two minutes.
         probe = run_oracle(args.workload, 256, 0.0, 1, warmup=1)
         per_row = probe["seconds_per_layer_sample"] / 256
         budget = 120.0 / max(1, args.steps + args.warmup)
         rows = int(max(64, min(w.n_tokens, budget / max(per_row, 1e-9))))
         res = run_oracle(args.workload, rows, 0.0, args.steps, warmup=args.warmup)
+        if res["reps"] != args.steps:
+            raise RuntimeError(f"oracle ran {res['reps']} timed reps, not {args.steps}")
         t = res["seconds_per_layer_sample"]
         value = rows / (t * s.n_layers)
-        sample = (f"1 layer x {rows} tokens of the {w.name} workload per step, extrapolated "
-                  f"to all {s.n_layers} layers (cost is linear in tokens and layers)")
+        sample = (f"1 layer x {rows} tokens of the {w.name} workload per step "
+                  f"({res['reps']} timed reps after {args.warmup} untimed), throughput "
+                  f"extrapolated to all {s.n_layers} layers (cost is linear in tokens and layers)")
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+                "ms_per_step": t * 1e3,
+                "ms_per_step_is": f"one timed rep: 1 layer x {rows} tokens",
+                "extrapolated_to_layers": s.n_layers,
+                "timed_seconds": res["seconds_total"],
+                "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": workload_desc},
+                "config": config,
                 "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": res["cores"],
                                  "kind": "oracle", "sample": sample},
                 "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -860,6 +1021,15 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     res = gpu_arm(args, rank, world, local_rank)
+    targets = None
+    run_targets = (args.targets != "off" and world == 1 and not args.layers and
+                   (args.targets != "auto" or args.workload == "llama2-7b"))
+    if run_targets:
+        import torch
+        gc.collect()
+        torch.cuda.empty_cache()
+        only = None if args.targets == "auto" else set(args.targets.split(","))
+        targets = targets_leg(torch.device("cuda", local_rank), peaks, peak_kind, only)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -918,19 +1088,9 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": s.dtype, "data": "synthetic",
-        "config": {"workload": workload_desc,
-                   "project_variant": ({0: "auto", 1: "single", 2: "pair"}[args.variant]
-                                       + f" -> {({1: 'single CTAs', 2: 'CTA pairs'}).get(res['variant'], '?')}"),
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": f"inputs larger than L2 ({(hid_b + w_b + kv_b) / 1e9:.2f} GB "
-                         "moved per step vs 129 MB L2); no flush",
-                   **({"layer_windows": f"{len(res['windows'])} windows of "
-                                        f"{res['windows'][0][1] - res['windows'][0][0]} layers "
-                                        "restored back to back per step; hidden states and "
-                                        "caches of all layers exceed HBM, so one window of "
-                                        "buffers is allocated and every window reads and "
-                                        "writes it"}
-                      if len(res["windows"]) > 1 else {})},
+        "config": config,
+        "project_variant": ({0: "auto", 1: "single", 2: "pair"}[args.variant]
+                            + f" -> {({1: 'single CTAs', 2: 'CTA pairs'}).get(res['variant'], '?')}"),
         "kv_gbs": kv_gbs,
         "step_roofline_frac": roof_t / t,
         "stage_ms": {"prepare": res["prep_ms"], "project": res["proj_ms"]},
@@ -957,6 +1117,7 @@ def main():
                  "plain_h2d_gbs": res["h2d_gbs"]}
                 if res["e2e_s"] == res["e2e_s"] else None),
         "gpu_launches": res["launches"],
+        "targets": targets,
         "clocks": res["clocks"],
         "context": ({"torch_composite_ms_per_step": res["torch_ctx"],
                      "library_speedup": res["torch_ctx"] / (t * 1e3),

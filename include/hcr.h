@@ -483,8 +483,10 @@ hcr_status hcr_restore_streamed_encoded(hcr_handle* h, const hcr_codec_params* p
  * layers per call).  The handle's device must be current.
  *
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Every call on a device shares the one array,
+ * (cudaGetSymbolAddress) with that device current, and looks it up again
+ * whenever the current CUDA context differs from the one of the last lookup
+ * (after cudaDeviceReset, say, the array may sit elsewhere); make the first
+ * call in each context before any stream capture.  Every call on a device shares the one array,
  * which keeps the last call's contents; nothing in it needs to start at
  * zero (each restore writes every scratch word it later reads).  Calls
  * whose GPU work can overlap -- on different streams, or from different
@@ -501,12 +503,6 @@ hcr_status hcr_restore_no_alloc(hcr_handle* h, const void* hidden, int32_t layer
                                 void* stream);
 
 /*
- * hcr_check_device_error -- synchronise `stream`, then read and clear the
- * handle's device error word.  Returns HCR_OK, HCR_ERR_DEVICE_BOUNDS or
- * HCR_ERR_TIMEOUT (timeout wins), or HCR_ERR_CUDA if the synchronisation
- * failed.  The raw HCR_DEVERR_* bits go to *flags when flags is not NULL.
- */
-/*
  * hcr_project_variant -- the tile variant the projection of n_tokens tokens
  * over n_layers layers uses: 1 for single CTAs (128x256 tiles), 2 for CTA
  * pairs (256x256 tiles, cta_group::2).  Host-only; 0 for a NULL handle or
@@ -518,6 +514,12 @@ hcr_status hcr_restore_no_alloc(hcr_handle* h, const void* hidden, int32_t layer
  */
 int32_t hcr_project_variant(const hcr_handle* h, int32_t n_tokens, int32_t n_layers);
 
+/*
+ * hcr_check_device_error -- synchronise `stream`, then read and clear the
+ * handle's device error word.  Returns HCR_OK, HCR_ERR_DEVICE_BOUNDS or
+ * HCR_ERR_TIMEOUT (timeout wins), or HCR_ERR_CUDA if the synchronisation
+ * failed.  The raw HCR_DEVERR_* bits go to *flags when flags is not NULL.
+ */
 hcr_status hcr_check_device_error(hcr_handle* h, void* stream, uint32_t* flags);
 
 /*
@@ -537,10 +539,10 @@ hcr_status hcr_debug_set_stall(hcr_handle* h, int32_t enable);
 
 /*
  * hcr_debug_set_variant -- testing hook: which project-kernel variant later
- * restores through this handle use.  0 (default): automatic -- CTA pairs
- * (cta_group::2, 256-token tiles) for restores of more than 128 tokens,
- * single CTAs (128-token tiles) otherwise; 1: always single CTAs; 2: always
- * CTA pairs (HCR_ERR_UNSUPPORTED if the device cannot co-schedule them).
+ * restores through this handle use.  0 (default): automatic -- the choice
+ * hcr_project_variant reports for the call's token and layer counts; 1:
+ * always single CTAs (128-token tiles); 2: always CTA pairs (cta_group::2,
+ * 256-token tiles; HCR_ERR_UNSUPPORTED if the device cannot co-schedule them).
  * Both variants compute the same values bit for bit.  Do not change it while
  * a restore through the handle may be enqueued.
  */

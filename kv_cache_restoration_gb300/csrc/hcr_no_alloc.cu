@@ -12,9 +12,13 @@
 // library holds it until the process exits.
 //
 // Host code may not use the array's name as a device address (on the host it
-// names a stand-in object), so the address is looked up once per device with
-// cudaGetSymbolAddress, with that device current, and then passed to the
-// kernels like any caller-provided workspace.
+// names a stand-in object), so the address is looked up with
+// cudaGetSymbolAddress, with the handle's device current, and then passed to
+// the kernels like any caller-provided workspace.  The lookup is done once
+// per device and CUDA context: a context that is torn down and created again
+// (cudaDeviceReset, or a released primary context) loads the library's device
+// code again, possibly at another address, so the cached address is keyed on
+// the context's unique id and looked up again when that id changes.
 #include <mutex>
 
 #include "hcr_host.h"
@@ -25,8 +29,47 @@ namespace {
 static __device__ __align__(256) uint8_t g_restore_scratch[HCR_NO_ALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
+struct ScratchAddr {
+  unsigned long long ctx_id = 0;   // 0: not looked up yet
+  void* addr = nullptr;
+};
 std::mutex g_scratch_mutex;
-void* g_scratch_addr[kMaxDevices] = {};
+ScratchAddr g_scratch[kMaxDevices];
+
+// The unique id of the calling thread's current CUDA context (0 if none is
+// current yet), through the runtime's driver entry points, so the library
+// needs no link-time dependency on libcuda.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+hcr_status current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+    cudaGetLastError();
+  });
+  *id = 0;
+  if (!get_current || !get_id)
+    return set_last_error(HCR_ERR_CUDA, "driver entry points cuCtxGetCurrent/cuCtxGetId missing");
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS)
+    return set_last_error(HCR_ERR_CUDA, "cuCtxGetCurrent failed");
+  if (ctx && get_id(ctx, id) != CUDA_SUCCESS)
+    return set_last_error(HCR_ERR_CUDA, "cuCtxGetId failed");
+  return HCR_OK;
+}
 
 }  // namespace
 }  // namespace hcr
@@ -58,10 +101,16 @@ extern "C" hcr_status hcr_restore_no_alloc(hcr_handle* h, const void* hidden, in
                           h->impl.device);
   if (dev < 0 || dev >= kMaxDevices)
     return set_last_error(HCR_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, kMaxDevices);
+  unsigned long long ctx = 0;
+  hcr_status st = current_context_id(&ctx);
+  if (st != HCR_OK) return st;
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    ScratchAddr& c = g_scratch[dev];
+    if (ctx == 0 || c.ctx_id != ctx) {
+      // first call in this context (or no context current on this thread yet:
+      // the lookup makes the device's primary context current)
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_restore_scratch);
       if (e != cudaSuccess || !p) {
@@ -69,9 +118,11 @@ extern "C" hcr_status hcr_restore_no_alloc(hcr_handle* h, const void* hidden, in
         return set_last_error(HCR_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s",
                               cudaGetErrorString(e));
       }
-      g_scratch_addr[dev] = p;
+      if (ctx == 0 && (st = current_context_id(&ctx)) != HCR_OK) return st;
+      c.ctx_id = ctx;
+      c.addr = p;
     }
-    scratch = g_scratch_addr[dev];
+    scratch = c.addr;
   }
   return hcr_restore(h, hidden, layer_begin, layer_end, n_req, n_tokens, cu_seqlens, start_pos,
                      block_table, max_blocks_per_req, k_cache, v_cache, layout, scratch,

@@ -29,6 +29,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "restored tokens/s and KV GB/s written; % of bf16 tensor peak / HBM roofline"
+VARIANT_NAMES = {1: "single CTAs", 2: "CTA pairs", 3: "CTA pairs, weight rows as M"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -108,6 +109,7 @@ class ClockSampler:
 
 
 KERNEL_SOURCES = ["kv_cache_restoration_gb300/csrc/hcr_project.cu",
+                  "kv_cache_restoration_gb300/csrc/hcr_pipe.cuh",
                   "kv_cache_restoration_gb300/csrc/ptx.cuh",
                   "kv_cache_restoration_gb300/csrc/hcr_internal.h"]
 
@@ -590,8 +592,7 @@ def targets_leg(device, peaks, peak_kind, only=None):
             "steps": steps, "warmup": warmup, "timed_s": total_s,
             "ms_per_step": t_step * 1e3, "tokens_per_s": T / t_step,
             "stage_ms": {"prepare": prep_ms, "project": proj_ms},
-            "project_variant": {1: "single CTAs", 2: "CTA pairs"}.get(
-                B.hcr_project_variant(r.handle, T, L), "?"),
+            "project_variant": VARIANT_NAMES.get(B.hcr_project_variant(r.handle, T, L), "?"),
             "roofline": roof, "clocks": clocks,
             "target": target, "met": None if target is None else bool(roof["frac"] >= target),
         }
@@ -940,7 +941,8 @@ def main():
                     help="restore in windows of this many layers (0: all at once; default: 8 "
                          "for the ragged batch, whose buffers exceed HBM, else all at once)")
     ap.add_argument("--variant", type=int, default=0,
-                    help="project kernel tiles: 0 automatic, 1 single CTAs, 2 CTA pairs")
+                    help="project kernel tiles: 0 automatic, 1 single CTAs, 2 CTA pairs, "
+                         "3 CTA pairs with weight rows as M (tokens as N)")
     ap.add_argument("--layers", type=int, default=0,
                     help="cut the model to its first N layers (small profiling cases)")
     ap.add_argument("--targets", default="auto",
@@ -1089,8 +1091,8 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": s.dtype, "data": "synthetic",
         "config": config,
-        "project_variant": ({0: "auto", 1: "single", 2: "pair"}[args.variant]
-                            + f" -> {({1: 'single CTAs', 2: 'CTA pairs'}).get(res['variant'], '?')}"),
+        "project_variant": ({0: "auto", 1: "single", 2: "pair", 3: "weight rows"}[args.variant]
+                            + f" -> {VARIANT_NAMES.get(res['variant'], '?')}"),
         "kv_gbs": kv_gbs,
         "step_roofline_frac": roof_t / t,
         "stage_ms": {"prepare": res["prep_ms"], "project": res["proj_ms"]},

@@ -505,8 +505,11 @@ hcr_status hcr_restore_no_alloc(hcr_handle* h, const void* hidden, int32_t layer
 /*
  * hcr_project_variant -- the tile variant the projection of n_tokens tokens
  * over n_layers layers uses: 1 for single CTAs (128x256 tiles), 2 for CTA
- * pairs (256x256 tiles, cta_group::2).  Host-only; 0 for a NULL handle or
- * empty sizes.  The choice, made from measurements on GB300: pairs when
+ * pairs (256x256 tiles, cta_group::2), 3 for CTA pairs with the weight rows
+ * as the MMA's M side (two 128-wide heads) and a chunk of tokens as its N side
+ * (tokens padded to a multiple of 16 instead of 128 rows; 128-wide heads
+ * only).  Host-only; 0 for a NULL handle or empty sizes.  The choice, made
+ * from measurements on GB300: 3 for 257..320 tokens; otherwise pairs when
  * there is more than one 128-row tile of tokens, d_model <= 4096, padding to
  * 128-row tiles saves less than 10% of the rows that 256-row tiles pad, and
  * the call is at most 32 TFLOP (4 d_model d_kv n_tokens n_layers); single
@@ -542,8 +545,10 @@ hcr_status hcr_debug_set_stall(hcr_handle* h, int32_t enable);
  * restores through this handle use.  0 (default): automatic -- the choice
  * hcr_project_variant reports for the call's token and layer counts; 1:
  * always single CTAs (128-token tiles); 2: always CTA pairs (cta_group::2,
- * 256-token tiles; HCR_ERR_UNSUPPORTED if the device cannot co-schedule them).
- * Both variants compute the same values bit for bit.  Do not change it while
+ * 256-token tiles; HCR_ERR_UNSUPPORTED if the device cannot co-schedule them);
+ * 3: always CTA pairs with weight rows as M (HCR_ERR_UNSUPPORTED unless
+ * head_dim is 128 and the pairs can be co-scheduled).
+ * All variants compute the same values bit for bit.  Do not change it while
  * a restore through the handle may be enqueued.
  */
 hcr_status hcr_debug_set_variant(hcr_handle* h, int32_t variant);

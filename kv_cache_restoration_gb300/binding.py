@@ -427,7 +427,8 @@ def hcr_check_device_error(handle, stream=None):
 
 
 def hcr_project_variant(handle, n_tokens: int, n_layers: int) -> int:
-    """Tile variant the projection uses: 1 single CTAs, 2 CTA pairs (host-only)."""
+    """Tile variant the projection uses: 1 single CTAs, 2 CTA pairs, 3 CTA pairs
+    with weight rows as M and chunks of up to 320 tokens as N (host-only)."""
     return lib.hcr_project_variant(handle, n_tokens, n_layers)
 
 
@@ -443,7 +444,8 @@ def hcr_debug_timeout_record(handle, stream=None):
 
 
 def hcr_debug_set_variant(handle, variant: int) -> int:
-    """Testing hook: 0 automatic, 1 single-CTA tiles, 2 CTA-pair tiles."""
+    """Testing hook: 0 automatic, 1 single-CTA tiles, 2 CTA-pair tiles, 3 CTA-pair
+    tiles with weight rows as M (128-wide heads only)."""
     return lib.hcr_debug_set_variant(handle, variant)
 
 

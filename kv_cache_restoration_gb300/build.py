@@ -19,10 +19,11 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhcr.so")
 
-SOURCES = ["hcr_api.cu", "hcr_prepare.cu", "hcr_project.cu", "hcr_no_alloc.cu",
+SOURCES = ["hcr_api.cu", "hcr_prepare.cu", "hcr_project.cu", "hcr_project_swap.cu",
+           "hcr_no_alloc.cu",
            "hcr_streamed.cu", "hcr_save.cu", "hcr_kv.cu", "hcr_plan.cu",
            "hcr_codec.cu"]
-HEADERS = ["hcr_internal.h", "hcr_host.h", "ptx.cuh"]
+HEADERS = ["hcr_internal.h", "hcr_host.h", "hcr_pipe.cuh", "ptx.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

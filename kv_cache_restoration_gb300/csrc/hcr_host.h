@@ -28,8 +28,12 @@ struct Handle {
   CUtensorMap tmap_w;          // 3-D map over w_packed: (d, 2*d_kv, L), box (64, 256, 1)
   CUtensorMap tmap_w_half;     // same tensor, box (64, 128, 1): half a tile per CTA of a pair
   int pair_clusters = 0;       // co-resident CTA pairs of the pair variant (0: unavailable)
+  // Weight-row tiles (head_dim 128 only): 5-D view of w_packed, dims (d, 8, 2,
+  // 8, L * 2 * n_kv_heads) with row strides (1, 64, 8, 128), box (64, 8, 2, 8, 1)
+  CUtensorMap tmap_w5;
+  int swap_clusters = 0;       // co-resident CTA pairs of that kernel (0: unavailable)
   uint32_t debug_stall = 0;    // test hook: see hcr_debug_set_stall
-  int32_t variant = 0;         // test hook: 0 auto, 1 single CTAs, 2 CTA pairs
+  int32_t variant = 0;         // test hook: 0 auto, 1 single CTAs, 2 CTA pairs, 3/4 weight rows
   StreamedRes* streamed = nullptr;  // created on the first hcr_restore_streamed call
 };
 

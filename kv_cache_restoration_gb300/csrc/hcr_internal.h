@@ -23,7 +23,7 @@ constexpr int kBlockK = 64;            // 64 x 2 bytes = one 128-byte swizzle ro
 constexpr int kUmmaK = 16;             // K of one tcgen05.mma kind::f16
 constexpr int kStages = 4;             // TMA -> MMA ring depth, single-CTA variant (48 KB stages)
 constexpr int kStagesPair = 7;         // ring depth per CTA, CTA-pair variant (32 KB stages)
-constexpr int kStagesMax = 7;
+constexpr int kStagesMax = 10;         // barrier slots in the pipeline state (any variant)
 constexpr int kAccums = 2;             // TMEM accumulators (epilogue overlaps next mainloop)
 constexpr int kTileBytesA = kBlockM * kBlockK * 2;
 constexpr int kTileBytesB = kBlockN * kBlockK * 2;
@@ -36,6 +36,29 @@ constexpr size_t kSmemSingle = size_t(kStages) * kStageBytes + 1024;
 constexpr size_t kSmemPair = size_t(kStagesPair) * (kTileBytesA + kTileBytesB / 2) + 1024;
 static_assert(kSmemSingle <= 232448 - 512 && kSmemPair <= 232448 - 512,
               "ring does not fit the 227 KB of shared memory a CTA can use");
+// Weight-row tiles (tokens as the MMA's N side, CTA pairs): a ring of stages
+// of 16 KB of weights plus chunk/2 token rows (128 B each) per CTA, as many as
+// fit (at most kStagesMax), 8 epilogue warps, and a 1 KB transpose buffer
+// (two blocks) per epilogue warp.  Short chunks get deeper rings: in the weight-streaming
+// regime the ring depth sets how many weight bytes are in flight from HBM.
+constexpr int kSwapEpilogueWarps = 8;
+constexpr int kSwapThreads = 64 + 32 * kSwapEpilogueWarps;
+// TMEM holds a ring of accumulator slots, one MMA's N each: two slots of 256
+// columns (a tile of up to 256 tokens takes one), or three of 160 (a tile of
+// up to 320 tokens takes two).
+constexpr int kSwapSlotsMax = 3;
+constexpr int kSwapTmemCols = 512;     // allocated (a power of two >= the ring)
+constexpr int kSwapMaxChunk = 320;     // tokens per tile (three-slot ring)
+constexpr size_t kSmemSwap = 232448 - 1024;   // dynamic shared memory of the kernel
+constexpr size_t kSwapStaging = size_t(kSwapEpilogueWarps) * 1024;
+// per-token table of a tile for the epilogue: rstd, mean, position (4 B each)
+// and slot (8 B) of up to 512 tokens
+constexpr size_t kSwapTokenTable = 512 * (4 + 4 + 4 + 8);
+inline int swap_stages(int chunk) {
+  const size_t stage = size_t(kTileBytesA) + size_t(chunk / 2) * kBlockK * 2;
+  const size_t n = (kSmemSwap - 1024 - kSwapStaging - kSwapTokenTable) / stage;
+  return int(n < size_t(kStagesMax) ? n : size_t(kStagesMax));
+}
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded pipeline waits: 2 s
 // The device error word is followed, at this word offset, by a record of the
 // first bounded wait that gave up: {which wait, CTA, thread, a, b, parity}.
@@ -123,6 +146,12 @@ struct ProjectParams {
   int32_t row_elems;      // n_kv_heads * head_dim
   uint32_t* err;
   uint32_t debug_stall;
+  // Weight-row tiles only: tiles are (layer, head pair, token chunk); chunks
+  // hold `chunk` tokens (a multiple of 16, at most kSwapMaxChunk) except the
+  // last, which holds last_n (a multiple of 16, at most chunk).
+  int32_t chunk, n_chunks, last_n, head_pairs;
+  int32_t stages;   // ring depth (swap_stages(chunk))
+  int32_t slot_cols, n_slots;   // TMEM accumulator ring: 2 x 256 or 3 x 160 columns
 };
 
 // Launchers (return cudaGetLastError() of the launch).
@@ -133,6 +162,12 @@ cudaError_t launch_project(const CUtensorMap& tmap_h, const CUtensorMap& tmap_h6
                            cudaStream_t s);
 // Co-resident clusters of the CTA-pair variant on the current device (< 0 on error).
 int project_pair_clusters(int dtype);
+// Weight-row tiles: tmap_h has boxes of chunk/2 token rows; tmap_w5 is the 5-D
+// view of the packed weights (box = one head's 128 rows, reordered so that
+// each rotate-half pair shares a thread in the epilogue).  grid is even.
+cudaError_t launch_project_swap(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w5,
+                                const ProjectParams& p, int grid, cudaStream_t s);
+int project_swap_clusters(int dtype);
 cudaError_t launch_pack_weights(const void* w_k, const void* w_v, const void* gamma, void* dst,
                                 int d_kv, int d, int dtype, cudaStream_t s);
 cudaError_t launch_column_constants(const void* w_packed, const void* w_k, const void* w_v,

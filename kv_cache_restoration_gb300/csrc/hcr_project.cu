@@ -38,10 +38,13 @@
 #include <cuda_fp16.h>
 
 #include "hcr_internal.h"
+#include "hcr_pipe.cuh"
 #include "ptx.cuh"
 
 namespace hcr {
 namespace {
+
+using namespace pipe;
 
 struct TileCoord {
   int l, m, n;
@@ -62,84 +65,6 @@ __device__ __forceinline__ TileCoord tile_coord(int64_t tile, const ProjectParam
   c.m = g * kGroupM + within % rows;
   c.n = within / rows;
   return c;
-}
-
-struct __align__(8) PipeState {
-  uint64_t full[kStagesMax];    // TMA -> MMA: stage filled
-  uint64_t empty[kStagesMax];   // MMA -> TMA: stage consumed
-  uint64_t tfull[kAccums];   // MMA -> epilogue: accumulator complete
-  uint64_t tempty[kAccums];  // epilogue -> MMA: accumulator drained
-  uint64_t drain;            // MMA completion on shutdown
-  uint32_t tmem_base;
-  int32_t abort;
-};
-
-// Records where a bounded wait gave up (first one wins): which wait, the CTA
-// and thread, and two call-site values (tile index, k-block or accumulator).
-__device__ __forceinline__ void record_timeout(const ProjectParams& p, uint32_t code,
-                                               uint32_t a, uint32_t b, uint32_t parity) {
-  atomicOr(p.err, uint32_t(HCR_DEVERR_TIMEOUT));
-  uint32_t* d = p.err + kDiagOffset;
-  if (atomicCAS(d, 0u, code) == 0u) {
-    d[1] = blockIdx.x;
-    d[2] = threadIdx.x;
-    d[3] = a;
-    d[4] = b;
-    d[5] = parity;
-    __threadfence();
-  }
-}
-
-// Waits for the phase of `bar` with the given parity.  Gives up when another
-// role raised the abort flag or after kWaitLimitNs, raising it itself.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int32_t* abort,
-                                           const ProjectParams& p, uint32_t code, uint32_t a,
-                                           uint32_t b) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
-  while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      record_timeout(p, code, a, b, parity);
-      return false;
-    }
-  }
-}
-
-// Bounded wait used only while shutting down after an abort.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = ptx::globaltimer_ns();
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs / 4) return;
-  }
-}
-
-template <int DT>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  if constexpr (DT == HCR_DTYPE_BF16) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  } else {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  }
-}
-
-template <int DT>
-__device__ __forceinline__ void store16(uint16_t* dst, const float (&x)[16]) {
-  uint4 lo, hi;
-  lo.x = pack2<DT>(x[0], x[1]);
-  lo.y = pack2<DT>(x[2], x[3]);
-  lo.z = pack2<DT>(x[4], x[5]);
-  lo.w = pack2<DT>(x[6], x[7]);
-  hi.x = pack2<DT>(x[8], x[9]);
-  hi.y = pack2<DT>(x[10], x[11]);
-  hi.z = pack2<DT>(x[12], x[13]);
-  hi.w = pack2<DT>(x[14], x[15]);
-  reinterpret_cast<uint4*>(dst)[0] = lo;
-  reinterpret_cast<uint4*>(dst)[1] = hi;
 }
 
 // Per-variant tiling.  Single: one CTA computes a 128x256 tile with
@@ -401,18 +326,14 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
           const int ca = col0 + j, cb = col0 + half + j;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            float xa = __uint_as_float(ra[i]);
-            float xb = __uint_as_float(rb[i]);
-            if (p.layer_norm) {
-              xa = rstd * (xa - mean * __ldg(csum + ca + i));
-              xb = rstd * (xb - mean * __ldg(csum + cb + i));
-            } else {
-              xa *= rstd;
-              xb *= rstd;
-            }
+            const bool ln = p.layer_norm;
+            float xa = norm_scale(__uint_as_float(ra[i]), rstd, mean,
+                                  ln ? __ldg(csum + ca + i) : 0.f, ln);
+            float xb = norm_scale(__uint_as_float(rb[i]), rstd, mean,
+                                  ln ? __ldg(csum + cb + i) : 0.f, ln);
             if (cbias) {
-              xa += __ldg(cbias + ca + i);
-              xb += __ldg(cbias + cb + i);
+              xa = __fadd_rn(xa, __ldg(cbias + ca + i));
+              xb = __fadd_rn(xb, __ldg(cbias + cb + i));
             }
             a[i] = xa;
             b[i] = xb;
@@ -423,12 +344,8 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float4 cs = __ldg(tab + i);   // (cos, sin) of pairs j+2i, j+2i+1
-              const float a0 = a[2 * i], b0 = b[2 * i];
-              const float a1 = a[2 * i + 1], b1 = b[2 * i + 1];
-              a[2 * i] = a0 * cs.x - b0 * cs.y;
-              b[2 * i] = b0 * cs.x + a0 * cs.y;
-              a[2 * i + 1] = a1 * cs.z - b1 * cs.w;
-              b[2 * i + 1] = b1 * cs.z + a1 * cs.w;
+              rope_pair(a[2 * i], b[2 * i], cs.x, cs.y);
+              rope_pair(a[2 * i + 1], b[2 * i + 1], cs.z, cs.w);
             }
           }
           if (valid) {

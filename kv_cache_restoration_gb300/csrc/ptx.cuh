@@ -148,6 +148,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+// 16 lanes x 256 bits (8 columns): thread i of the warp gets columns 2(i%4)
+// and 2(i%4)+1 of TMEM lane (base + i/4) in r[0], r[1], and of lane
+// (base + 8 + i/4) in r[2], r[3] -- the register layout of an 8x8 matrix
+// fragment (row i/4, two adjacent columns), twice.
+__device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -204,6 +214,33 @@ __device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst_smem, const v
       : "memory");
 }
 
+// 5-D tiled tensor load into this CTA's shared memory, completion counted on an
+// mbarrier in either CTA of the pair (the weight rows of the weight-row tiles
+// come through a 5-D view that reorders them inside the box).
+__device__ __forceinline__ void tma_load_5d_pair(uint32_t dst_smem, const void* tmap,
+                                                 uint32_t bar_cluster, int32_t c0, int32_t c1,
+                                                 int32_t c2, int32_t c3, int32_t c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".cta_group::2 [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst_smem),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "r"(c4)
+      : "memory");
+}
+
+// Same, with an L2 eviction-priority hint (a createpolicy value).
+__device__ __forceinline__ void tma_load_5d_pair_hint(uint32_t dst_smem, const void* tmap,
+                                                      uint32_t bar_cluster, int32_t c0, int32_t c1,
+                                                      int32_t c2, int32_t c3, int32_t c4,
+                                                      uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".cta_group::2.L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst_smem),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "r"(c4), "l"(policy)
+      : "memory");
+}
+
 // One warp of each CTA of the pair executes these together.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -241,6 +278,30 @@ __device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar, uint16_t
       " [%0], %1;" ::"r"(bar),
       "h"(cta_mask)
       : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Shared memory: transposing stores and vector loads
+// ---------------------------------------------------------------------------
+// Four 8x8 matrices of 16-bit elements, each held as a fragment (thread i:
+// row i/4, columns 2(i%4) and 2(i%4)+1 packed in one register), stored
+// transposed: row k of matrix m (its column k, 16 bytes) goes to the address
+// thread 8m + k passes.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr, uint32_t r0, uint32_t r1,
+                                                  uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(
+                   addr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 
 // ---------------------------------------------------------------------------

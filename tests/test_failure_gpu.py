@@ -8,14 +8,24 @@ import pytest
 
 from tests import harness as Hn
 from workloads import configs as C
+from workloads.configs import ModelShape, Workload
 
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("variant", [1, 2], ids=["single", "pair"])
-def test_stalled_pipeline_times_out_and_context_survives(cuda_device, variant):
+# the weight-row tiles need 128-wide heads: 1-layer cases with two of them,
+# one with a single-MMA chunk (129 tokens) and one with a two-MMA chunk (300)
+HEAD128 = {"weight-rows": Workload("stall128", ModelShape("s128", 1, 256, 2, 2, 128), (129,),
+                                   (2,)),
+           "weight-rows-2mma": Workload("stall128x2", ModelShape("s128", 1, 256, 2, 2, 128),
+                                        (300,), (2,))}
+
+
+@pytest.mark.parametrize("name", ["single", "pair", "weight-rows", "weight-rows-2mma"])
+def test_stalled_pipeline_times_out_and_context_survives(cuda_device, name):
     from kv_cache_restoration_gb300 import binding as B
-    w = C.get("tiny")
+    variant = {"single": 1, "pair": 2}.get(name, 3)
+    w = HEAD128[name] if variant == 3 else C.get("tiny")
     case = Hn.make_case(w, cuda_device)
     assert B.hcr_debug_set_variant(case.restorer.handle, variant) == B.HCR_OK
     assert B.hcr_debug_set_stall(case.restorer.handle, True) == B.HCR_OK

@@ -16,7 +16,7 @@ from workloads.configs import ModelShape, Workload
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = (0, 1, 2)   # automatic, single CTAs, CTA pairs
+VARIANTS = (0, 1, 2, 3)   # automatic, single CTAs, CTA pairs, weight-row CTA pairs
 
 
 def _case(seed: int):
@@ -38,7 +38,10 @@ def _case(seed: int):
     w = Workload(f"fuzz{seed}", shape, lens, starts, block_size=rng.choice((1, 8, 16, 32, 64)),
                  block_order=rng.choice(("contiguous", "shuffled")),
                  spare_blocks=rng.randint(0, 4), seed=seed)
-    return w, VARIANTS[seed % 3]
+    variant = VARIANTS[seed % 4]
+    if variant >= 3 and head_dim != 128:     # weight-row tiles need 128-wide heads
+        variant = 0
+    return w, variant
 
 
 @pytest.mark.parametrize("seed", range(40))

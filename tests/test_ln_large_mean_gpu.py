@@ -80,13 +80,15 @@ def _errors_by_mean(case, rows=None):
     return out
 
 
-@pytest.mark.parametrize("variant", ["auto", "single", "pair"])
+@pytest.mark.parametrize("variant", ["auto", "single", "pair", "swap"])
 @pytest.mark.parametrize("w", CASES, ids=[w.name for w in CASES])
 def test_large_row_means(cuda_device, w, variant):
     from kv_cache_restoration_gb300 import binding as B
+    if variant.startswith("swap") and w.shape.head_dim != 128:
+        pytest.skip("weight-row tiles need 128-wide heads")
     case = Hn.make_case(w, cuda_device)
-    assert B.hcr_debug_set_variant(case.restorer.handle, {"auto": 0, "single": 1,
-                                                          "pair": 2}[variant]) == 0
+    assert B.hcr_debug_set_variant(case.restorer.handle, {"auto": 0, "single": 1, "pair": 2,
+                                                          "swap": 3}[variant]) == 0
     Hn.run(case)
     assert case.status == 0, (case.status, case.flags)
     Hn.compare(case)                       # every element, every slot

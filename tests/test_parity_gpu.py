@@ -53,7 +53,7 @@ SMALL_CASES = [
 ]
 
 
-VARIANTS = {"auto": 0, "single": 1, "pair": 2}
+VARIANTS = {"auto": 0, "single": 1, "pair": 2, "swap": 3}
 
 
 @pytest.mark.parametrize("variant", list(VARIANTS))
@@ -61,26 +61,36 @@ VARIANTS = {"auto": 0, "single": 1, "pair": 2}
 def test_small_full(cuda_device, w, variant):
     from kv_cache_restoration_gb300 import binding as B
     case = Hn.make_case(w, cuda_device)
-    assert B.hcr_debug_set_variant(case.restorer.handle, VARIANTS[variant]) == 0
+    st = B.hcr_debug_set_variant(case.restorer.handle, VARIANTS[variant])
+    if variant.startswith("swap") and w.shape.head_dim != 128:
+        assert st == B.HCR_ERR_UNSUPPORTED      # weight-row tiles need 128-wide heads
+        return
+    assert st == 0
     Hn.run(case)
     assert case.status == 0, (case.status, case.flags)
     Hn.compare(case)
 
 
-def test_variants_agree(cuda_device):
-    """Single-CTA and CTA-pair tiles restore the same values (compared bit for
-    bit; a difference would show as a count of differing elements)."""
+AGREE_CASES = [SMALL_CASES[1], SMALL_CASES[4], SMALL_CASES[6], SMALL_CASES[11]]
+
+
+@pytest.mark.parametrize("w", AGREE_CASES, ids=[w.name for w in AGREE_CASES])
+def test_variants_agree(cuda_device, w):
+    """Single-CTA, CTA-pair and weight-row tiles restore the same values
+    (compared bit for bit; a difference would show as a count of differing
+    elements): RMSNorm and LayerNorm with bias, bf16 and fp16, GQA, RoPE."""
     from kv_cache_restoration_gb300 import binding as B
-    w = SMALL_CASES[1]
     a = Hn.make_case(w, cuda_device)
     B.hcr_debug_set_variant(a.restorer.handle, 1)
     Hn.run(a)
-    b = Hn.make_case(w, cuda_device, params=a.params, restorer=a.restorer)
-    B.hcr_debug_set_variant(b.restorer.handle, 2)
-    Hn.run(b)
-    for c in ("k_cache", "v_cache"):
-        diff = int((getattr(a, c).view(torch.int16) != getattr(b, c).view(torch.int16)).sum())
-        assert diff == 0, f"{c}: {diff} elements differ between variants"
+    for v in (2, 3):
+        b = Hn.make_case(w, cuda_device, params=a.params, restorer=a.restorer)
+        assert B.hcr_debug_set_variant(b.restorer.handle, v) == 0
+        Hn.run(b)
+        assert b.status == 0
+        for c in ("k_cache", "v_cache"):
+            diff = int((getattr(a, c).view(torch.int16) != getattr(b, c).view(torch.int16)).sum())
+            assert diff == 0, f"variant {v}, {c}: {diff} elements differ from single CTAs"
 
 
 def test_empty_restore_is_a_noop(cuda_device):
@@ -293,10 +303,10 @@ def test_variant_policy_decisions(cuda_device):
                                   shape.rope_theta, 16384, shape.dtype, shape.kv_bias), params)
     r7 = handle(LLAMA2_7B)
     h = r7.handle
-    # 300 and 794 tokens end in a half tail tile (<= 128 rows), so pairs pad no
-    # more than single CTAs there
-    want = {(64, 32): 1, (128, 32): 1, (256, 32): 2, (300, 32): 2, (500, 32): 2, (794, 32): 2,
-            (4096, 32): 2, (4096, 4): 2, (16384, 32): 1, (629259, 8): 1}
+    # weight rows as M (3) for 257..320 tokens, where token-row tiles pad most
+    want = {(64, 32): 1, (128, 32): 1, (256, 32): 2, (257, 32): 3, (300, 32): 3, (320, 32): 3,
+            (321, 32): 2, (500, 32): 2, (794, 32): 2, (4096, 32): 2, (4096, 4): 2,
+            (16384, 32): 1, (629259, 8): 1}
     assert {k: B.hcr_project_variant(h, *k) for k in want} == want
     assert B.hcr_project_variant(h, 0, 32) == 0
     assert B.hcr_debug_set_variant(h, 2) == 0
@@ -305,3 +315,6 @@ def test_variant_policy_decisions(cuda_device):
     assert B.hcr_project_variant(h, 4096, 32) == 1
     r13 = handle(LLAMA2_13B)
     assert B.hcr_project_variant(r13.handle, 4096, 40) == 1     # d_model 5120
+    assert B.hcr_project_variant(r13.handle, 300, 40) == 3
+    assert B.hcr_debug_set_variant(h, 3) == 0
+    assert B.hcr_project_variant(h, 4096, 32) == 3

@@ -227,25 +227,34 @@ hcr_status do_prepare(hcr_handle* h, const RestoreArgs& a, bool stats = true) {
   return HCR_OK;
 }
 
-// Tile variant of a projection of n_tokens tokens over n_layers layers
-// (true: CTA pairs), chosen from measurements on GB300:
-//   * CTA pairs (256-row tiles) once there is more than one 128-row tile of
-//     tokens: they do ~8-12% more work per clock, and weight-streaming
-//     restores of 129-256 tokens run ~15% faster with them;
-//   * single CTAs for short restores (one 128-row tile of tokens), which
-//     would only pad the pair's second half;
-//   * single CTAs where 128-row tiles pad at least 10% fewer rows than the
-//     pairs' tiles: the padding saved outweighs the lower rate.  With the
-//     half tail (below) pairs pad no more than single CTAs unless heads are
-//     wider than 128 columns;
-//   * single CTAs for models wider than 4096: at d_model 5120 and 7168 they
-//     ran 4-5% faster in long power-capped restores and no slower at
-//     2-4K tokens, while at 4096 pairs win by 5-7%;
-//   * single CTAs for calls of more than 32 TFLOP: pairs draw more power per
-//     clock, and in long calls the power cap pulls their clock further down
-//     (a 629K-token batch in 8-layer calls of 338 TFLOP: single CTAs 10%
-//     faster; 35 TFLOP calls: a tie; 8.8 TFLOP calls: pairs 5.5% faster).
-// The debug hook (hcr_debug_set_variant) overrides the choice.
+// The automatic tile-variant choice, one table.  Every threshold comes from a
+// measurement on GB300 (project kernel time, CUDA events); for a new shape,
+// re-derive it with `bench.py --workload <shape>-T<n> --variant 1|2|3` at the
+// token counts around it.
+struct VariantPolicy {
+  // CTA pairs need more than one 128-row tile of tokens: at 64 and 128 tokens
+  // single CTAs ran 0.337 / 0.348 ms, and pairs only pad their second half.
+  int32_t pair_min_tokens = kBlockM + 1;
+  // Widths above 4096: single CTAs ran 4-5% faster on the 13B (5120) and
+  // OPT-30B (7168) shapes in long power-capped restores and no slower at
+  // 2-4K tokens; at 4096 the pairs win by 5-7%.
+  int32_t pair_max_d_model = 4096;
+  // Calls above 32 TFLOP (4 d_model d_kv tokens layers): pairs draw more power
+  // per clock and the cap pulls their clock down (629K tokens in 8-layer calls
+  // of 338 TFLOP: single CTAs 10% faster; 35 TFLOP: a tie; 8.8: pairs 5.5%).
+  double pair_max_call_flops = 32e12;
+  // Single CTAs where their 128-row tiles pad at least 10% fewer rows than
+  // the pairs' 256-row tiles (counting the pairs' half tail tile as 128 rows).
+  double pair_pad_ratio = 0.9;
+  // Weight rows as M for 257..320 tokens (one chunk of up to 320 on the
+  // three-slot TMEM ring): 7B 0.526 against 0.576 ms (pairs), 13B 0.974
+  // against 1.080 (single CTAs), OPT-30B 2.33 against 2.54 ms (single CTAs);
+  // from 384 tokens the token-row pairs were 5-10% faster.
+  int32_t rows_min_tokens = kBlockN + 1;
+  int32_t rows_max_tokens = kSwapMaxChunk;
+};
+constexpr VariantPolicy kPolicy{};
+
 // A pair projection can end each layer with an M=128 "half tail" tile (64
 // rows per CTA) when the last 256-row tile holds at most 128 rows; its
 // epilogue splits a row's 256 columns in two 128-column halves, so heads must
@@ -264,8 +273,10 @@ bool use_pairs(const Handle& H, int32_t n_tokens, int32_t n_layers) {
   const int64_t pad_pair = (int64_t(n_tokens) + 2 * kBlockM - 1) / (2 * kBlockM) * (2 * kBlockM) -
                            (half_tail_fits(d, n_tokens) ? kBlockM : 0);
   const double call_flops = 4.0 * d.d_model * double(d_kv) * double(n_tokens) * n_layers;
-  bool pair = H.pair_clusters > 0 && n_tokens > kBlockM && d.d_model <= 4096 &&
-              10 * pad128 > 9 * pad_pair && call_flops <= 32e12;
+  bool pair = H.pair_clusters > 0 && n_tokens >= kPolicy.pair_min_tokens &&
+              d.d_model <= kPolicy.pair_max_d_model &&
+              double(pad128) > kPolicy.pair_pad_ratio * double(pad_pair) &&
+              call_flops <= kPolicy.pair_max_call_flops;
   if (H.variant == 1) pair = false;
   if (H.variant == 2) pair = H.pair_clusters > 0;
   return pair;
@@ -300,17 +311,13 @@ SwapPlan swap_plan(int32_t n_tokens) {
 
 bool swap_available(const Handle& H) { return H.swap_clusters > 0; }
 
-// Tile variant of a projection: 1 single CTAs, 2 CTA pairs (token rows as M),
-// 3 CTA pairs with weight rows as M and chunks of tokens as N.  The weight
-// rows take restores of 257..320 tokens (one 304-column chunk at 300 tokens,
-// where 128-row tiles compute 384 rows and 256-row tiles 512), on every model
-// width measured: 7B 0.526 against 0.576 ms (pairs), 13B 0.974 against 1.080
-// (single CTAs), OPT-30B 2.33 against 2.54 ms (single CTAs).  From 384 tokens
-// up the token-row pairs were 5-10% faster on the 7B shape.
+// Tile variant of a projection (kPolicy): 1 single CTAs, 2 CTA pairs (token
+// rows as M), 3 CTA pairs with weight rows as M and chunks of tokens as N.
 int32_t choose_variant(const Handle& H, int32_t n_tokens, int32_t n_layers) {
   const bool swap_ok = swap_available(H) && swap_plan(n_tokens).ok;
   int32_t v = use_pairs(H, n_tokens, n_layers) ? 2 : 1;
-  if (swap_ok && n_tokens > kBlockN && n_tokens <= kSwapMaxChunk) v = 3;
+  if (swap_ok && n_tokens >= kPolicy.rows_min_tokens && n_tokens <= kPolicy.rows_max_tokens)
+    v = 3;
   if (H.variant == 1) v = 1;
   if (H.variant == 2) v = H.pair_clusters > 0 ? 2 : 1;
   if (H.variant == 3 && swap_ok) v = 3;

@@ -28,6 +28,30 @@ def test_full_size(cuda_device, name):
     Hn.compare(case, rows=Hn.sample_rows(w, 1 / 64), check_sentinel=True)  # every layer
 
 
+@pytest.mark.parametrize("name", ["llama2-7b-T300", "llama2-13b-T300", "opt-30b-T300",
+                                  "llama2-7b-T794"])
+def test_full_size_short_restores(cuda_device, name):
+    """The short restores the bench times beside the headline, at full model
+    size and in its launch configuration: 300 tokens run on the weight-row
+    tiles (the automatic choice for 257..320 tokens), 794 on token-row tiles.
+    Every row of every layer is checked (the oracle is cheap at 300-800 rows),
+    plus the sentinel check on every slot."""
+    from kv_cache_restoration_gb300 import binding as B
+    w = C.get(name)
+    L = w.shape.n_layers
+    case = Hn.make_case(w, cuda_device, gen_device=cuda_device)
+    want = 3 if w.n_tokens == 300 else None
+    if want is not None:
+        assert B.hcr_project_variant(case.restorer.handle, w.n_tokens, L) == want
+    lay = case.layout
+    for stage in ("prepare", "project"):
+        case.restorer.restore(case.hidden, 0, L, case.cu, case.start, case.table, case.k_cache,
+                              case.v_cache, lay.num_blocks, lay.block_size, stage=stage)
+    case.status, case.flags = case.restorer.check()
+    assert case.status == 0, (case.status, case.flags)
+    Hn.compare(case, check_sentinel=True)
+
+
 def test_ragged_batch_in_layer_windows(cuda_device):
     """64 requests, ~648K tokens, ragged lengths and starts, permuted block
     table.  Hidden states plus caches for all 32 layers exceed HBM, so the

@@ -109,6 +109,7 @@ class ClockSampler:
 
 
 KERNEL_SOURCES = ["kv_cache_restoration_gb300/csrc/hcr_project.cu",
+                  "kv_cache_restoration_gb300/csrc/hcr_epilogue.cuh",
                   "kv_cache_restoration_gb300/csrc/hcr_pipe.cuh",
                   "kv_cache_restoration_gb300/csrc/ptx.cuh",
                   "kv_cache_restoration_gb300/csrc/hcr_internal.h"]
@@ -128,7 +129,8 @@ def profiled_traffic(workload_base: str, n_layers: int):
                 h.update(f.read())
     except OSError:
         return None
-    if rec.get("source_sha256_16") != h.hexdigest()[:16] or rec.get("workload_base") != workload_base:
+    if (rec.get("source_sha256_16") != h.hexdigest()[:16]
+            or rec.get("workload_base") != workload_base):
         return None
     return (rec["dram_bytes_read"] + rec["dram_bytes_write"]) * n_layers / rec["captured_layers"]
 
@@ -342,123 +344,168 @@ def gpu_arm(args, rank, world, local_rank):
     hidden_host = case.hidden.cpu().pin_memory() if e2e_steps > 0 else None
     meta_host = [t.cpu().pin_memory() for t in (case.cu, case.start, case.table)]
     meta_dev = [case.cu, case.start, case.table]
-    h2d = (hidden_host.numel() * hidden_host.element_size() if e2e_steps > 0 else 0) + sum(
-        m.numel() * m.element_size() for m in meta_host)
+    meta_bytes = sum(m.numel() * m.element_size() for m in meta_host)
     chunk = max(1, min(args.e2e_chunk, L))
-    chunk_bytes = chunk * T * s.d_model * 2
-    staging = torch.empty(args.e2e_slots * chunk_bytes if e2e_steps > 0 else 256,
-                          dtype=torch.uint8, device=device)
     layout = B.hcr_cache_layout(lay.num_blocks, lay.block_size, 0)
-    src = None
-    if args.e2e_source == "chunks" and e2e_steps > 0:
-        # The saved form: 64-token chunks [chunk][layer][row][d] in pinned host
-        # memory, written once by the save kernel before the timed region.
-        import dataclasses
-        import numpy as np
-        clay = G.request_layout(dataclasses.replace(w, block_size=args.e2e_chunk_tokens))
-        ctab_np = np.ascontiguousarray(clay.block_table, dtype=np.int32)
-        store = torch.empty((clay.num_blocks, L, args.e2e_chunk_tokens, s.d_model),
-                            dtype=case.hidden.dtype).pin_memory()
-        ctab = torch.as_tensor(ctab_np, device=device)
-        B.hcr_save_hidden(r.handle, case.hidden, 0, L, w.n_req, T, case.cu, case.start, ctab,
-                          int(ctab.shape[1]), args.e2e_chunk_tokens, store, clay.num_blocks,
-                          stream)
-        torch.cuda.synchronize(device)
-        cu_np = np.ascontiguousarray(lay.cu_seqlens, dtype=np.int32)
-        start_np = np.ascontiguousarray(lay.start_pos, dtype=np.int32)
-        src = B.hcr_chunk_source(store.data_ptr(), args.e2e_chunk_tokens, clay.num_blocks,
-                                 ctab_np.ctypes.data, int(ctab_np.shape[1]), cu_np.ctypes.data,
-                                 start_np.ctypes.data)
-        src._keep = (store, ctab_np, cu_np, start_np)
-    split_plan = None
-    if args.e2e_source == "split" and e2e_steps > 0:
-        # Bubble-free layer split: profile the per-layer costs on this GPU,
-        # plan, and keep the upper layers' K/V (as the restore left them in
-        # the cache) in pinned host memory; the lower layers stay hidden states.
-        costs = B.hcr_profile_layer_costs(r.handle, T, chunk, 5, stream)
-        split_plan = B.hcr_plan_layer_split(costs, L)
-        if args.split_layer >= 0:
-            n_kv = L - min(args.split_layer, L)
-        else:
-            n_kv = split_plan.kv_layers
-        split = L - n_kv
-        d_kv = s.n_kv_heads * s.head_dim
-        kv_host = torch.empty((max(n_kv, 1), 2, T, d_kv), dtype=case.hidden.dtype).pin_memory()
-        if n_kv:
-            B.hcr_save_kv(r.handle, kv_host, split, L, w.n_req, T, case.cu, case.start, case.table,
-                          lay.max_blocks, case.k_cache[split:], case.v_cache[split:], layout, ws,
-                          ws.numel(), stream)
-        torch.cuda.synchronize(device)
-        hid_host_split = hidden_host[:max(split, 1)]
-        slot_bytes = max(min(chunk, split) * T * s.d_model * 2 if split else 0,
-                         2 * T * d_kv * 2 if n_kv else 0)
-        staging = torch.empty(args.e2e_slots * slot_bytes, dtype=torch.uint8, device=device)
-        h2d = (split * T * s.d_model + n_kv * 2 * T * d_kv) * 2 + sum(
-            m.numel() * m.element_size() for m in meta_host)
-        split_plan = dict(kv_layers=n_kv, hidden_layers=split,
-                          planned_kv_layers=split_plan.kv_layers,
-                          predicted_ms=split_plan.predicted_s * 1e3,
-                          costs_ms_per_layer={f: getattr(costs, f) * 1e3 for f in
-                                              ("restore_s", "hidden_copy_s", "kv_copy_s",
-                                               "kv_place_s")})
-    enc = None
-    if args.e2e_source == "encoded" and e2e_steps > 0:
-        # The codec's encoded form (int8 codes + anchor scales) in pinned host
-        # memory, written once by the encode kernel before the timed region.
-        params = B.codec_params()
-        codes_h = torch.empty((L, T, s.d_model), dtype=torch.int8).pin_memory()
-        scales_h = torch.zeros((L, T), dtype=torch.float32).pin_memory()
-        B.hcr_encode_hidden(r.handle, params, case.hidden, 0, L, w.n_req, T, case.cu, codes_h,
-                            scales_h, stream)
-        torch.cuda.synchronize(device)
-        staging = torch.empty(B.encoded_staging_bytes(T, s.d_model, chunk, args.e2e_slots),
-                              dtype=torch.uint8, device=device)
-        h2d = codes_h.numel() + scales_h.numel() * 4 + sum(
-            m.numel() * m.element_size() for m in meta_host)
-        enc = (params, codes_h, scales_h)
-    t0 = time.perf_counter()
-    step_s = []
-    ew = args.e2e_warmup
-    # Each step waits on the host, so a pause of this process would land in
-    # the step's time: collect once here and keep the cyclic collector off
-    # while the leg runs.
-    gc.collect()
-    gc.disable()
-    for i in range(ew + e2e_steps if e2e_steps > 0 else 0):
-        if i == ew:
+
+    def e2e_leg(source):
+        """One end-to-end leg from the host form `source`: per-step times (s),
+        host-to-device bytes per step, and the split plan (split only)."""
+        staging = torch.empty(args.e2e_slots * chunk * T * s.d_model * 2, dtype=torch.uint8,
+                              device=device)
+        h2d = hidden_host.numel() * hidden_host.element_size() + meta_bytes
+        src = split_plan = enc = None
+        if source == "chunks":
+            # The saved form: 64-token chunks [chunk][layer][row][d] in pinned
+            # host memory, written once by the save kernel before the timed region.
+            import dataclasses
+            import numpy as np
+            clay = G.request_layout(dataclasses.replace(w, block_size=args.e2e_chunk_tokens))
+            ctab_np = np.ascontiguousarray(clay.block_table, dtype=np.int32)
+            store = torch.empty((clay.num_blocks, L, args.e2e_chunk_tokens, s.d_model),
+                                dtype=case.hidden.dtype).pin_memory()
+            ctab = torch.as_tensor(ctab_np, device=device)
+            B.hcr_save_hidden(r.handle, case.hidden, 0, L, w.n_req, T, case.cu, case.start,
+                              ctab, int(ctab.shape[1]), args.e2e_chunk_tokens, store,
+                              clay.num_blocks, stream)
             torch.cuda.synchronize(device)
-            t0 = time.perf_counter()
-        ts = time.perf_counter()
-        for hm, dm in zip(meta_host, meta_dev):
-            dm.copy_(hm, non_blocking=True)
+            cu_np = np.ascontiguousarray(lay.cu_seqlens, dtype=np.int32)
+            start_np = np.ascontiguousarray(lay.start_pos, dtype=np.int32)
+            src = B.hcr_chunk_source(store.data_ptr(), args.e2e_chunk_tokens, clay.num_blocks,
+                                     ctab_np.ctypes.data, int(ctab_np.shape[1]),
+                                     cu_np.ctypes.data, start_np.ctypes.data)
+            src._keep = (store, ctab_np, cu_np, start_np)
+        if source == "split":
+            # Bubble-free layer split: profile the per-layer costs on this GPU,
+            # plan, and keep the upper layers' K/V (as the restore left them in
+            # the cache) in pinned host memory; the lower layers stay hidden states.
+            costs = B.hcr_profile_layer_costs(r.handle, T, chunk, 5, stream)
+            plan = B.hcr_plan_layer_split(costs, L)
+            n_kv = L - min(args.split_layer, L) if args.split_layer >= 0 else plan.kv_layers
+            split = L - n_kv
+            d_kv = s.n_kv_heads * s.head_dim
+            kv_host = torch.empty((max(n_kv, 1), 2, T, d_kv), dtype=case.hidden.dtype).pin_memory()
+            if n_kv:
+                B.hcr_save_kv(r.handle, kv_host, split, L, w.n_req, T, case.cu, case.start,
+                              case.table, lay.max_blocks, case.k_cache[split:],
+                              case.v_cache[split:], layout, ws, ws.numel(), stream)
+            torch.cuda.synchronize(device)
+            hid_host_split = hidden_host[:max(split, 1)]
+            slot_bytes = max(min(chunk, split) * T * s.d_model * 2 if split else 0,
+                             2 * T * d_kv * 2 if n_kv else 0)
+            staging = torch.empty(args.e2e_slots * slot_bytes, dtype=torch.uint8, device=device)
+            h2d = (split * T * s.d_model + n_kv * 2 * T * d_kv) * 2 + meta_bytes
+            split_plan = dict(kv_layers=n_kv, hidden_layers=split,
+                              planned_kv_layers=plan.kv_layers,
+                              predicted_ms=plan.predicted_s * 1e3,
+                              costs_ms_per_layer={f: getattr(costs, f) * 1e3 for f in
+                                                  ("restore_s", "hidden_copy_s", "kv_copy_s",
+                                                   "kv_place_s")})
+        if source == "encoded":
+            # The codec's encoded form (int8 codes + anchor scales) in pinned
+            # host memory, written once by the encode kernel before the timed
+            # region; each group is restored straight from its codes.
+            params = B.codec_params()
+            codes_h = torch.empty((L, T, s.d_model), dtype=torch.int8).pin_memory()
+            scales_h = torch.zeros((L, T), dtype=torch.float32).pin_memory()
+            B.hcr_encode_hidden(r.handle, params, case.hidden, 0, L, w.n_req, T, case.cu,
+                                codes_h, scales_h, stream)
+            torch.cuda.synchronize(device)
+            staging = torch.empty(B.encoded_staging_bytes(T, s.d_model, chunk, args.e2e_slots),
+                                  dtype=torch.uint8, device=device)
+            h2d = codes_h.numel() + scales_h.numel() * 4 + meta_bytes
+            enc = (params, codes_h, scales_h)
+        step_s = []
+        ew = args.e2e_warmup
+        # Each step waits on the host, so a pause of this process would land in
+        # the step's time: collect once here and keep the cyclic collector off
+        # while the leg runs.
+        gc.collect()
+        gc.disable()
+        t0 = time.perf_counter()
+        for i in range(ew + e2e_steps):
+            if i == ew:
+                torch.cuda.synchronize(device)
+                t0 = time.perf_counter()
+            ts = time.perf_counter()
+            for hm, dm in zip(meta_host, meta_dev):
+                dm.copy_(hm, non_blocking=True)
+            if enc is not None:
+                B.hcr_restore_streamed_encoded(r.handle, enc[0], enc[1], enc[2], 0, L, w.n_req,
+                                               T, case.cu, case.start, case.table,
+                                               lay.max_blocks, case.k_cache, case.v_cache,
+                                               layout, staging, staging.numel(), chunk, ws,
+                                               ws.numel(), stream)
+            elif split_plan is not None:
+                B.hcr_restore_streamed_split(r.handle, hid_host_split, kv_host, 0,
+                                             split_plan["hidden_layers"], L, w.n_req, T,
+                                             case.cu, case.start, case.table, lay.max_blocks,
+                                             case.k_cache, case.v_cache, layout, staging,
+                                             staging.numel(), chunk, ws, ws.numel(), stream)
+            elif src is None:
+                B.hcr_restore_streamed(r.handle, hidden_host, 0, L, w.n_req, T, case.cu,
+                                       case.start, case.table, lay.max_blocks, case.k_cache,
+                                       case.v_cache, layout, staging, staging.numel(), chunk,
+                                       ws, ws.numel(), stream)
+            else:
+                B.hcr_restore_streamed_chunks(r.handle, src, 0, L, w.n_req, T, case.cu,
+                                              case.start, case.table, lay.max_blocks,
+                                              case.k_cache, case.v_cache, layout, staging,
+                                              staging.numel(), chunk, ws, ws.numel(), stream)
+            st, _ = r.check(stream)          # syncs and reads the 4-byte status word
+            if st != 0:
+                raise RuntimeError(f"device error in the {source} end-to-end leg")
+            if i >= ew:
+                step_s.append(time.perf_counter() - ts)
+        total = (time.perf_counter() - t0) / e2e_steps
+        gc.enable()
+        del staging
+        device_ms = None
         if enc is not None:
-            B.hcr_restore_streamed_encoded(r.handle, enc[0], enc[1], enc[2], 0, L, w.n_req, T,
-                                           case.cu, case.start, case.table, lay.max_blocks,
-                                           case.k_cache, case.v_cache, layout, staging,
-                                           staging.numel(), chunk, ws, ws.numel(), stream)
-        elif split_plan is not None:
-            B.hcr_restore_streamed_split(r.handle, hid_host_split, kv_host, 0,
-                                         split_plan["hidden_layers"], L, w.n_req, T, case.cu,
-                                         case.start, case.table, lay.max_blocks, case.k_cache,
-                                         case.v_cache, layout, staging, staging.numel(), chunk,
-                                         ws, ws.numel(), stream)
-        elif src is None:
-            B.hcr_restore_streamed(r.handle, hidden_host, 0, L, w.n_req, T, case.cu,
-                                   case.start, case.table, lay.max_blocks, case.k_cache,
-                                   case.v_cache, layout, staging, staging.numel(), chunk, ws,
-                                   ws.numel(), stream)
-        else:
-            B.hcr_restore_streamed_chunks(r.handle, src, 0, L, w.n_req, T, case.cu, case.start,
-                                          case.table, lay.max_blocks, case.k_cache,
-                                          case.v_cache, layout, staging, staging.numel(), chunk,
-                                          ws, ws.numel(), stream)
-        st, _ = r.check(stream)          # syncs and reads the 4-byte status word
-        if st != 0:
-            raise RuntimeError("device error in e2e leg")
-        if i >= ew:
-            step_s.append(time.perf_counter() - ts)
-    e2e_s = (time.perf_counter() - t0) / e2e_steps if e2e_steps > 0 else float("nan")
-    gc.enable()
+            # beside it, both routes with the codes already in HBM (all layers,
+            # CUDA events on the stream): the decode kernel then the restore,
+            # and hcr_restore_encoded, which decodes inside the projection
+            codes_d, scales_d = enc[1].to(device), enc[2].to(device)
+            ews = torch.empty(max(B.hcr_encoded_workspace_bytes(r.handle, T, L), 256),
+                              dtype=torch.uint8, device=device)
+            dec = torch.empty_like(case.hidden)
+
+            def decode_then_restore():
+                B.hcr_decode_hidden(r.handle, enc[0], codes_d, scales_d, 0, L, w.n_req, T,
+                                    case.cu, dec, stream)
+                r.restore(dec, 0, L, case.cu, case.start, case.table, case.k_cache,
+                          case.v_cache, lay.num_blocks, lay.block_size, stream=stream,
+                          workspace=ws)
+
+            def decode_in_gemm():
+                B.hcr_restore_encoded(r.handle, enc[0], codes_d, scales_d, 0, L, w.n_req, T,
+                                      case.cu, case.start, case.table, lay.max_blocks,
+                                      case.k_cache, case.v_cache, layout, ews, ews.numel(),
+                                      stream)
+
+            device_ms = {}
+            n_dev = max(3, min(args.steps, 20))
+            for name, fn in (("decode_then_restore", decode_then_restore),
+                             ("decode_in_gemm", decode_in_gemm)):
+                for _ in range(3):
+                    fn()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(n_dev):
+                    fn()
+                e1.record(stream)
+                torch.cuda.synchronize(device)
+                device_ms[name] = e0.elapsed_time(e1) / n_dev
+            if r.check(stream)[0] != 0:
+                raise RuntimeError("device error in the encoded restores")
+            del codes_d, scales_d, ews, dec
+        return dict(s=total, steps=step_s, h2d=h2d, split=split_plan, device_ms=device_ms)
+
+    legs = {}
+    if e2e_steps > 0:
+        legs["e2e"] = e2e_leg(args.e2e_source)
+        if args.e2e_encoded and args.e2e_source != "encoded":
+            legs["e2e_encoded"] = e2e_leg("encoded")
     # context: one plain copy of all hidden states, host to device
     h2d_gbs = None
     if e2e_steps > 0:
@@ -474,17 +521,52 @@ def gpu_arm(args, rank, world, local_rank):
         torch_ctx = torch_composite_ms(w, case, device, stream)
 
     t_step = total_ms / 1e3 / args.steps
-    e2e_med = statistics.median(step_s) if step_s else float("nan")
-    e2e_p90 = sorted(step_s)[int(0.9 * (len(step_s) - 1))] if step_s else float("nan")
-    e2e_max = max(step_s) if step_s else float("nan")
-    t_step, proj_ms, prep_ms, e2e_s, e2e_med, e2e_p90, e2e_max = reduce_max_over_ranks(
-        [t_step, proj_ms, prep_ms, e2e_s, e2e_med, e2e_p90, e2e_max], device)
-    return dict(w=w, t_step=t_step, proj_ms=proj_ms, prep_ms=prep_ms, e2e_s=e2e_s, h2d=h2d,
+    t_step, proj_ms, prep_ms = reduce_max_over_ranks([t_step, proj_ms, prep_ms], device)
+    for leg in legs.values():
+        if leg["device_ms"] is not None:
+            names = sorted(leg["device_ms"])
+            leg["device_ms"] = dict(zip(names, reduce_max_over_ranks(
+                [leg["device_ms"][n] for n in names], device)))
+        st_ = leg.pop("steps")
+        leg["s"], leg["median_s"], leg["p90_s"], leg["max_s"] = reduce_max_over_ranks(
+            [leg["s"], statistics.median(st_), sorted(st_)[int(0.9 * (len(st_) - 1))],
+             max(st_)], device)
+    return dict(w=w, t_step=t_step, proj_ms=proj_ms, prep_ms=prep_ms, legs=legs,
                 clocks=clk.summary(), launches=2 * nw * args.steps, windows=windows,
-                h2d_gbs=h2d_gbs, chunk=chunk,
-                split=split_plan, torch_ctx=torch_ctx,
-                variant=B.hcr_project_variant(r.handle, T, windows[0][1] - windows[0][0]),
-                e2e_median_s=e2e_med, e2e_p90_s=e2e_p90, e2e_max_s=e2e_max)
+                h2d_gbs=h2d_gbs, chunk=chunk, torch_ctx=torch_ctx,
+                variant=B.hcr_project_variant(r.handle, T, windows[0][1] - windows[0][0]))
+
+
+E2E_API = {
+    "layers": "hcr_restore_streamed, {chunk}-layer chunks, ",
+    "chunks": "hcr_restore_streamed_chunks from a pinned host store of {chunk_tokens}-token "
+              "chunks, {chunk}-layer groups, ",
+    "split": "hcr_restore_streamed_split (hidden states below the split, saved K/V above), "
+             "{chunk}-layer groups, ",
+    "encoded": "hcr_restore_streamed_encoded (int8 anchor + delta codes and anchor scales, "
+               "about half the bytes; each group decoded by the decode kernel on a second "
+               "stream, then restored), groups of 1, 2, 4 ... up to {chunk} layers, ",
+}
+
+
+def e2e_record(res, key, source, args, world, w):
+    """The JSON record of one end-to-end leg (None when it did not run)."""
+    leg = res["legs"].get(key)
+    if leg is None:
+        return None
+    return {"value": whole_job_tokens_per_s(world, w.n_tokens, leg["s"]), "unit": "tokens/s",
+            "h2d_bytes_per_step": leg["h2d"], "d2h_bytes_per_step": 4,
+            "ms_per_step": leg["s"] * 1e3,
+            "ms_per_step_median": leg["median_s"] * 1e3,
+            "ms_per_step_p90": leg["p90_s"] * 1e3,
+            "ms_per_step_max": leg["max_s"] * 1e3,
+            "steps": min(args.steps, args.e2e_steps), "warmup": args.e2e_warmup,
+            "api": E2E_API[source].format(chunk=res["chunk"],
+                                          chunk_tokens=args.e2e_chunk_tokens)
+            + f"{args.e2e_slots}-slot staging ring",
+            "layer_split": leg["split"],
+            "device_ms_per_step_codes_in_hbm": leg["device_ms"],
+            "plain_h2d_gbs": res["h2d_gbs"]}
 
 
 # The north-star targets beside the headline: each workload restored through
@@ -937,6 +1019,9 @@ def main():
     ap.add_argument("--split-layer", type=int, default=-1,
                     help="with --e2e-source split: first K/V layer (default: the planner's)")
     ap.add_argument("--e2e-chunk-tokens", type=int, default=64, help="tokens per saved chunk")
+    ap.add_argument("--e2e-encoded", type=int, default=1,
+                    help="1: also time the end-to-end leg from the codec's encoded form "
+                         "(the line's e2e_encoded key)")
     ap.add_argument("--window-layers", type=int, default=-1,
                     help="restore in windows of this many layers (0: all at once; default: 8 "
                          "for the ragged batch, whose buffers exceed HBM, else all at once)")
@@ -1098,26 +1183,8 @@ def main():
         "stage_ms": {"prepare": res["prep_ms"], "project": res["proj_ms"]},
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": ({"value": whole_job_tokens_per_s(world, w.n_tokens, res["e2e_s"]),
-                 "unit": "tokens/s",
-                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": 4,
-                 "ms_per_step": res["e2e_s"] * 1e3,
-                 "ms_per_step_median": res["e2e_median_s"] * 1e3,
-                 "ms_per_step_p90": res["e2e_p90_s"] * 1e3,
-                 "ms_per_step_max": res["e2e_max_s"] * 1e3,
-                 "steps": args.e2e_steps, "warmup": args.e2e_warmup,
-                 "api": {"layers": f"hcr_restore_streamed, {res['chunk']}-layer chunks, ",
-                         "chunks": f"hcr_restore_streamed_chunks from a pinned host store of "
-                                   f"{args.e2e_chunk_tokens}-token chunks, {res['chunk']}-layer "
-                                   "groups, ",
-                         "split": f"hcr_restore_streamed_split (hidden states below the split, "
-                                  f"saved K/V above), {res['chunk']}-layer groups, ",
-                         "encoded": f"hcr_restore_streamed_encoded (int8 anchor + delta codes, "
-                                    f"decoded on the GPU), {res['chunk']}-layer groups, "}[
-                            args.e2e_source] + f"{args.e2e_slots}-slot staging ring",
-                 "layer_split": res["split"],
-                 "plain_h2d_gbs": res["h2d_gbs"]}
-                if res["e2e_s"] == res["e2e_s"] else None),
+        "e2e": e2e_record(res, "e2e", args.e2e_source, args, world, w),
+        "e2e_encoded": e2e_record(res, "e2e_encoded", "encoded", args, world, w),
         "gpu_launches": res["launches"],
         "targets": targets,
         "clocks": res["clocks"],

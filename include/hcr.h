@@ -435,6 +435,39 @@ hcr_status hcr_decode_hidden(hcr_handle* h, const hcr_codec_params* params, cons
                              void* hidden, void* stream);
 
 /*
+ * hcr_restore_encoded -- hcr_restore straight from the codec's encoded form
+ * in device memory, decoded inside the restore kernels (HCache episode, cues
+ * 30 and 32: restore from compressed hidden states; CacheGen review, section
+ * 核心方法: the anchor + delta groups):
+ *     codes  [layer_end - layer_begin][n_tokens][d_model] int8
+ *     scales [layer_end - layer_begin][n_tokens] float32
+ * as hcr_encode_hidden writes them with the same params.  The prepare kernel
+ * computes the norm statistics of the decoded rows and each token's group
+ * anchor; the projection (CTA pairs) loads the int8 codes with TMA and its
+ * converter warps decode each k-block into the MMA's operand in shared
+ * memory, so no decoded copy is written.  The caches are bit-identical to
+ * hcr_decode_hidden followed by hcr_restore with the same arguments.
+ *
+ * codes and scales must be device memory (codes 16-byte, scales 4-byte
+ * aligned); d_model must be a multiple of 16.  The workspace needs
+ * hcr_encoded_workspace_bytes(h, n_tokens, layer_end - layer_begin) bytes
+ * (the statistics plus 4 bytes per token).  Codec parameters are checked as
+ * in hcr_decode_hidden and the rest as in hcr_restore before anything is
+ * enqueued; HCR_ERR_UNSUPPORTED when the device fits no CTA pair of this
+ * kernel.  A token in no request is decoded as zeros and flagged
+ * HCR_DEVERR_SEQLENS; the other device-side checks are hcr_restore's.
+ */
+size_t hcr_encoded_workspace_bytes(const hcr_handle* h, int32_t n_tokens,
+                                   int32_t n_layers_in_range);
+hcr_status hcr_restore_encoded(hcr_handle* h, const hcr_codec_params* params, const void* codes,
+                               const void* scales, int32_t layer_begin, int32_t layer_end,
+                               int32_t n_req, int32_t n_tokens, const int32_t* cu_seqlens,
+                               const int32_t* start_pos, const int32_t* block_table,
+                               int32_t max_blocks_per_req, void* k_cache, void* v_cache,
+                               const hcr_cache_layout* layout, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/*
  * hcr_restore_streamed_encoded -- hcr_restore_streamed from the codec's
  * encoded form in pinned host memory:
  *     codes_host  [layer_end - layer_begin][n_tokens][d_model] int8

@@ -137,6 +137,11 @@ lib.hcr_restore_streamed_encoded.argtypes = [_vp, ctypes.POINTER(hcr_codec_param
                                              _vp, ctypes.POINTER(hcr_cache_layout), _vp,
                                              ctypes.c_size_t, _i32, _vp, ctypes.c_size_t, _vp]
 lib.hcr_restore_streamed_encoded.restype = ctypes.c_int
+lib.hcr_encoded_workspace_bytes.argtypes = [_vp, _i32, _i32]
+lib.hcr_encoded_workspace_bytes.restype = ctypes.c_size_t
+lib.hcr_restore_encoded.argtypes = [_vp, ctypes.POINTER(hcr_codec_params), _vp, _vp] + \
+    _RESTORE_ARGTYPES[2:]
+lib.hcr_restore_encoded.restype = ctypes.c_int
 lib.hcr_restore_no_alloc.argtypes = _RESTORE_ARGTYPES[:13] + [_vp]
 lib.hcr_restore_no_alloc.restype = ctypes.c_int
 HCR_NO_ALLOC_SCRATCH_BYTES = 16 << 20
@@ -363,6 +368,26 @@ def hcr_decode_hidden(handle, params: hcr_codec_params, codes, scales, layer_beg
                                _ptr(hidden), _stream_ptr(stream))
     if check:
         _check(st, "hcr_decode_hidden")
+    return st
+
+
+def hcr_encoded_workspace_bytes(handle, n_tokens: int, n_layers_in_range: int) -> int:
+    return lib.hcr_encoded_workspace_bytes(handle, n_tokens, n_layers_in_range)
+
+
+def hcr_restore_encoded(handle, params: hcr_codec_params, codes, scales, layer_begin, layer_end,
+                        n_req, n_tokens, cu_seqlens, start_pos, block_table, max_blocks_per_req,
+                        k_cache, v_cache, layout, workspace, workspace_bytes, stream=None, *,
+                        check: bool = True) -> int:
+    """hcr_restore from the codec's encoded form in device memory, decoded
+    inside the restore kernels."""
+    st = lib.hcr_restore_encoded(
+        handle, ctypes.byref(params), _ptr(codes), _ptr(scales), layer_begin, layer_end, n_req,
+        n_tokens, _ptr(cu_seqlens), _ptr(start_pos), _ptr(block_table), max_blocks_per_req,
+        _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout) if layout is not None else None,
+        _ptr(workspace), workspace_bytes, _stream_ptr(stream))
+    if check:
+        _check(st, "hcr_restore_encoded")
     return st
 
 

@@ -20,10 +20,11 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhcr.so")
 
 SOURCES = ["hcr_api.cu", "hcr_prepare.cu", "hcr_project.cu", "hcr_project_swap.cu",
-           "hcr_no_alloc.cu",
+           "hcr_project_enc.cu", "hcr_no_alloc.cu",
            "hcr_streamed.cu", "hcr_save.cu", "hcr_kv.cu", "hcr_plan.cu",
            "hcr_codec.cu"]
-HEADERS = ["hcr_internal.h", "hcr_host.h", "hcr_pipe.cuh", "ptx.cuh"]
+HEADERS = ["hcr_internal.h", "hcr_host.h", "hcr_pipe.cuh", "hcr_epilogue.cuh",
+           "hcr_decode.cuh", "ptx.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

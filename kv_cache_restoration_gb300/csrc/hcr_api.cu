@@ -149,7 +149,8 @@ struct RestoreArgs {
 // whether the workspace must hold norm statistics for the layer range, not
 // only the slot map.
 hcr_status validate_restore(const hcr_handle* h, const RestoreArgs& a, bool* empty,
-                            bool stats = true, const char* input = "hidden") {
+                            bool stats = true, const char* input = "hidden",
+                            bool encoded = false) {
   *empty = false;
   if (!h) return fail(HCR_ERR_INVALID_ARG, "handle is NULL");
   const hcr_model_dims& d = h->impl.dims;
@@ -183,7 +184,7 @@ hcr_status validate_restore(const hcr_handle* h, const RestoreArgs& a, bool* emp
   if (a.layout->layer_stride_elems % 8)
     return fail(HCR_ERR_INVALID_ARG, "layer_stride_elems must be a multiple of 8");
   const size_t need = workspace_layout(a.n_tokens, stats ? a.layer_end - a.layer_begin : 0,
-                                       d.norm == HCR_NORM_LAYER).total;
+                                       d.norm == HCR_NORM_LAYER, encoded).total;
   if (!a.workspace) return fail(HCR_ERR_WORKSPACE, "workspace is NULL");
   if (!aligned(a.workspace, 256))
     return fail(HCR_ERR_WORKSPACE, "workspace must be 256-byte aligned");
@@ -193,12 +194,16 @@ hcr_status validate_restore(const hcr_handle* h, const RestoreArgs& a, bool* emp
 }
 
 // stats = false: the slot map only (the K/V row copies need no statistics).
-hcr_status do_prepare(hcr_handle* h, const RestoreArgs& a, bool stats = true) {
+// enc: the statistics of the rows decoded from the codec's form, and each
+// token's group anchor for the projection (a.hidden is then unused).
+hcr_status do_prepare(hcr_handle* h, const RestoreArgs& a, bool stats = true,
+                      const CodecInput* enc = nullptr) {
   NvtxRange range("hcr.prepare");
   const Handle& H = h->impl;
   const hcr_model_dims& d = H.dims;
   const int32_t nl = stats ? a.layer_end - a.layer_begin : 0;
-  const WorkspaceLayout w = workspace_layout(a.n_tokens, nl, d.norm == HCR_NORM_LAYER);
+  const WorkspaceLayout w =
+      workspace_layout(a.n_tokens, nl, d.norm == HCR_NORM_LAYER, enc != nullptr);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   PrepareParams p{};
   p.cu_seqlens = a.cu_seqlens;
@@ -222,6 +227,11 @@ hcr_status do_prepare(hcr_handle* h, const RestoreArgs& a, bool stats = true) {
   p.rstd = reinterpret_cast<float*>(ws + w.rstd_off);
   p.mean = p.layer_norm ? reinterpret_cast<float*>(ws + w.mean_off) : nullptr;
   p.err = H.err;
+  p.layer_begin = a.layer_begin;
+  if (enc) {
+    p.enc = *enc;
+    p.enc.anchor = reinterpret_cast<int32_t*>(ws + w.anchor_off);
+  }
   cudaError_t e = launch_prepare(p, a.stream);
   if (e != cudaSuccess) return cuda_fail(e, "prepare launch");
   return HCR_OK;
@@ -381,22 +391,15 @@ hcr_status do_project_swap(hcr_handle* h, const RestoreArgs& a) {
   return HCR_OK;
 }
 
-hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
-  NvtxRange range("hcr.project");
-  const Handle& H = h->impl;
+// Parameters of a token-row projection (single CTAs, CTA pairs, and the
+// pairs that decode the codec's form); `encoded` places the workspace's
+// statistics as the encoded restore lays them out.
+ProjectParams token_row_params(const Handle& H, const RestoreArgs& a, bool pair, bool encoded) {
   const hcr_model_dims& d = H.dims;
   const int32_t nl = a.layer_end - a.layer_begin;
-  const int32_t variant = choose_variant(H, a.n_tokens, nl);
-  if (variant == 3) return do_project_swap(h, a);
-  const WorkspaceLayout w = workspace_layout(a.n_tokens, nl, d.norm == HCR_NORM_LAYER);
+  const WorkspaceLayout w = workspace_layout(a.n_tokens, nl, d.norm == HCR_NORM_LAYER, encoded);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   const int32_t d_kv = d.n_kv_heads * d.head_dim;
-
-  CUtensorMap tmap_h;
-  hcr_status st = encode_3d(&tmap_h, a.hidden, d.dtype, uint64_t(d.d_model),
-                            uint64_t(a.n_tokens), uint64_t(nl), kBlockM, "hidden");
-  if (st != HCR_OK) return st;
-
   ProjectParams p{};
   p.n_tokens = a.n_tokens;
   p.d_model = d.d_model;
@@ -405,7 +408,6 @@ hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
   p.head_dim = d.head_dim;
   p.n_layers = nl;
   p.layer_begin = a.layer_begin;
-  const bool pair = variant == 2;
   const int tile_m = pair ? 2 * kBlockM : kBlockM;
   p.half_tail = pair && half_tail_fits(d, a.n_tokens);
   p.m_tiles = (a.n_tokens + tile_m - 1) / tile_m;
@@ -432,6 +434,24 @@ hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
   p.row_elems = d_kv;
   p.err = H.err;
   p.debug_stall = H.debug_stall;
+  return p;
+}
+
+hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
+  NvtxRange range("hcr.project");
+  const Handle& H = h->impl;
+  const hcr_model_dims& d = H.dims;
+  const int32_t nl = a.layer_end - a.layer_begin;
+  const int32_t variant = choose_variant(H, a.n_tokens, nl);
+  if (variant == 3) return do_project_swap(h, a);
+
+  CUtensorMap tmap_h;
+  hcr_status st = encode_3d(&tmap_h, a.hidden, d.dtype, uint64_t(d.d_model),
+                            uint64_t(a.n_tokens), uint64_t(nl), kBlockM, "hidden");
+  if (st != HCR_OK) return st;
+
+  const bool pair = variant == 2;
+  const ProjectParams p = token_row_params(H, a, pair, false);
   const int grid = pair ? 2 * int(std::min<int64_t>(p.num_tiles, H.pair_clusters))
                         : int(std::min<int64_t>(p.num_tiles, H.num_sms));
   CUtensorMap tmap_h64 = tmap_h;
@@ -443,6 +463,48 @@ hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
   cudaError_t e = launch_project(tmap_h, tmap_h64, pair ? H.tmap_w_half : H.tmap_w, p, grid,
                                  pair, a.stream);
   if (e != cudaSuccess) return cuda_fail(e, "project launch");
+  return HCR_OK;
+}
+
+// 4-D map of the codec's int8 codes [Lr][T][d] viewed as (16 codes, T rows,
+// d/16 column chunks, Lr layers): a box (16, kEncCodeRows, 4, 1) lands one
+// k-block's 64 codes of kEncCodeRows rows chunk-major in shared memory, each
+// 16-code chunk of the rows kEncCodeRows x 16 bytes after the previous one.
+// No swizzle; zero fill outside the tensor (the first tile's box starts at row
+// -kEncCodeHalo, a ragged last k-block's box ends past d/16).
+hcr_status encode_codes(CUtensorMap* map, const void* codes, uint64_t d, uint64_t rows,
+                        uint64_t layers) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(HCR_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[4] = {16, rows, d / 16, layers};
+  const cuuint64_t strides[3] = {d, 16, d * rows};
+  const cuuint32_t box[4] = {16, uint32_t(kEncCodeRows), uint32_t(kBlockK / 16), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(codes), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(HCR_ERR_CUDA, "tensor map for codes: CUresult %d", int(r));
+  return HCR_OK;
+}
+
+// The projection of a restore from the codec's form (CTA pairs whose
+// converter warps decode the A operand); enc.anchor is set from the workspace.
+hcr_status do_project_enc(hcr_handle* h, const RestoreArgs& a, const CodecInput& enc) {
+  NvtxRange range("hcr.project_encoded");
+  const Handle& H = h->impl;
+  const hcr_model_dims& d = H.dims;
+  const int32_t nl = a.layer_end - a.layer_begin;
+  CUtensorMap tmap_c;
+  hcr_status st = encode_codes(&tmap_c, enc.codes, uint64_t(d.d_model), uint64_t(a.n_tokens),
+                               uint64_t(nl));
+  if (st != HCR_OK) return st;
+  const ProjectParams p = token_row_params(H, a, true, true);
+  CodecInput e = enc;
+  const WorkspaceLayout w = workspace_layout(a.n_tokens, nl, d.norm == HCR_NORM_LAYER, true);
+  e.anchor = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a.workspace) + w.anchor_off);
+  const int grid = 2 * int(std::min<int64_t>(p.num_tiles, H.enc_clusters));
+  cudaError_t err = launch_project_enc(tmap_c, H.tmap_w_half, p, e, grid, a.stream);
+  if (err != cudaSuccess) return cuda_fail(err, "project launch (encoded input)");
   return HCR_OK;
 }
 
@@ -605,6 +667,9 @@ hcr_status hcr_create(const hcr_model_dims* dims, const void* const* gamma,
   // How many CTA pairs fit at once; without any, restores use single CTAs.
   H.pair_clusters = std::max(0, project_pair_clusters(d.dtype));
   cudaGetLastError();
+  // The same for the pairs that decode the codec's form (hcr_restore_encoded).
+  H.enc_clusters = std::max(0, project_enc_clusters(d.dtype));
+  cudaGetLastError();
   // Weight-row tiles need 128-wide heads (one head per CTA of a pair).
   if (d.head_dim == 128 && H.pair_clusters > 0 &&
       encode_w5(&H.tmap_w5, H.w_packed, d.dtype, uint64_t(d.d_model),
@@ -675,6 +740,69 @@ hcr_status hcr_restore(hcr_handle* h, const void* hidden, int32_t layer_begin, i
   st = do_prepare(h, a);
   if (st != HCR_OK) return st;
   return do_project(h, a);
+}
+
+size_t hcr_encoded_workspace_bytes(const hcr_handle* h, int32_t n_tokens,
+                                   int32_t n_layers_in_range) {
+  if (!h || n_tokens <= 0 || n_layers_in_range <= 0) return 0;
+  return workspace_layout(n_tokens, n_layers_in_range, h->impl.dims.norm == HCR_NORM_LAYER, true)
+      .total;
+}
+
+static bool device_memory(const void* ptr) {
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged;
+}
+
+hcr_status hcr_restore_encoded(hcr_handle* h, const hcr_codec_params* params, const void* codes,
+                               const void* scales, int32_t layer_begin, int32_t layer_end,
+                               int32_t n_req, int32_t n_tokens, const int32_t* cu_seqlens,
+                               const int32_t* start_pos, const int32_t* block_table,
+                               int32_t max_blocks_per_req, void* k_cache, void* v_cache,
+                               const hcr_cache_layout* layout, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  NvtxRange range("hcr_restore_encoded");
+  const void* hidden = codes;
+  HCR_RESTORE_ARGS;
+  bool empty = false;
+  hcr_status st = validate_restore(h, a, &empty, true, "codes", true);
+  if (st != HCR_OK || empty) return st;
+  if ((st = check_codec(h, params, layer_begin, layer_end, n_req, n_tokens, cu_seqlens,
+                        &empty)) != HCR_OK)
+    return st;
+  if (!scales || !aligned(scales, 4))
+    return fail(HCR_ERR_INVALID_ARG, "scales must be non-NULL and 4-byte aligned");
+  const Handle& H = h->impl;
+  if (H.dims.d_model % 16)
+    return fail(HCR_ERR_UNSUPPORTED,
+                "the encoded restore needs d_model a multiple of 16 (the codes' row pitch "
+                "for TMA), got %d", H.dims.d_model);
+  if (H.enc_clusters <= 0)
+    return fail(HCR_ERR_UNSUPPORTED, "no CTA pair of the encoded projection fits on this device");
+  if (!device_memory(codes) || !device_memory(scales))
+    return fail(HCR_ERR_INVALID_ARG, "codes and scales must be device memory");
+  CodecInput enc{};
+  enc.codes = static_cast<const int8_t*>(codes);
+  enc.scales = static_cast<const float*>(scales);
+  enc.cu_seqlens = cu_seqlens;
+  enc.n_req = n_req;
+  enc.group_tokens = params->group_tokens;
+  enc.n_layers_total = H.dims.n_layers;
+  for (int i = 0; i < 3; ++i) enc.bins[i] = params->bins[i];
+  // c * b exact for every code c in [-127, 127] and every bin: the projection
+  // may then add it with one fused multiply-add
+  enc.exact_products = 1;
+  for (float b : params->bins)
+    for (int c = -127; c <= 127; ++c)
+      if (const float prod = float(c) * b; double(prod) != double(c) * double(b))
+        enc.exact_products = 0;
+  st = do_prepare(h, a, true, &enc);
+  if (st != HCR_OK) return st;
+  return do_project_enc(h, a, enc);
 }
 
 static hcr_status kv_rows(hcr_handle* h, const RestoreArgs& a, bool to_cache, const char* what) {

@@ -32,6 +32,7 @@ struct Handle {
   // 8, L * 2 * n_kv_heads) with row strides (1, 64, 8, 128), box (64, 8, 2, 8, 1)
   CUtensorMap tmap_w5;
   int swap_clusters = 0;       // co-resident CTA pairs of that kernel (0: unavailable)
+  int enc_clusters = 0;        // co-resident CTA pairs decoding the codec's form (0: unavailable)
   uint32_t debug_stall = 0;    // test hook: see hcr_debug_set_stall
   int32_t variant = 0;         // test hook: 0 auto, 1 single CTAs, 2 CTA pairs, 3/4 weight rows
   StreamedRes* streamed = nullptr;  // created on the first hcr_restore_streamed call

@@ -1,4 +1,4 @@
-// Internal declarations the restore kernels (hcr_prepare.cu, hcr_project.cu)
+// Internal declarations the restore kernels (hcr_prepare.cu, hcr_project*.cu)
 // are compiled from: tiling constants, the instruction descriptor, the
 // workspace layout, kernel parameters and their launchers.  Host-only
 // declarations live in hcr_host.h.  Not part of the public ABI.
@@ -69,6 +69,9 @@ enum : uint32_t {
   kWaitMmaAccum = 3,        // a, b = tile, accumulator
   kWaitMmaFull = 4,         // a, b = tile, k-block
   kWaitEpilogueAccum = 7,   // a, b = tile, accumulator
+  kWaitCodesEmpty = 8,      // encoded input: code producer, a, b = tile, k-block
+  kWaitConvCodes = 9,       // encoded input: converter waits for codes, a, b = tile, k-block
+  kWaitConvStage = 10,      // encoded input: converter waits for a free A stage
 };
 
 // tcgen05 instruction descriptor for kind::f16, fp32 accumulate, both
@@ -84,12 +87,15 @@ constexpr uint32_t make_idesc_f16(int dtype, int m, int n) {
 // Workspace layout (all offsets 256-byte aligned)
 // ---------------------------------------------------------------------------
 struct WorkspaceLayout {
-  size_t slot_off, pos_off, rstd_off, mean_off, total;
+  size_t slot_off, pos_off, rstd_off, mean_off, anchor_off, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WorkspaceLayout workspace_layout(int64_t n_tokens, int64_t n_layers, bool layer_norm) {
+// encoded: a restore from the codec's form also keeps each token's group
+// anchor (int32 [T]) after the statistics.
+inline WorkspaceLayout workspace_layout(int64_t n_tokens, int64_t n_layers, bool layer_norm,
+                                        bool encoded = false) {
   WorkspaceLayout w{};
   size_t off = 0;
   w.slot_off = off;
@@ -100,6 +106,8 @@ inline WorkspaceLayout workspace_layout(int64_t n_tokens, int64_t n_layers, bool
   off = align_up(off + size_t(n_tokens) * size_t(n_layers) * 4, 256);
   w.mean_off = off;
   if (layer_norm) off = align_up(off + size_t(n_tokens) * size_t(n_layers) * 4, 256);
+  w.anchor_off = off;
+  if (encoded) off = align_up(off + size_t(n_tokens) * 4, 256);
   w.total = off;
   return w;
 }
@@ -107,6 +115,29 @@ inline WorkspaceLayout workspace_layout(int64_t n_tokens, int64_t n_layers, bool
 // ---------------------------------------------------------------------------
 // Kernel parameters
 // ---------------------------------------------------------------------------
+// The codec's encoded hidden states as the restore kernels read them
+// directly (hcr_restore_encoded): int8 codes and per-anchor-row scales of the
+// call's first layer, the request table that forms the anchor groups, the
+// group anchor of every token, and the layer-third bins.
+// Rows of codes a k-block's code stage holds before the tile's own rows (the
+// group anchors of the tile's first rows), and the rows it holds in all: the
+// tile's 128, the halo, and one more so that the stage's four 16-code column
+// chunks lie 145 rows of 16 bytes apart (an odd pitch, so that rows four apart
+// fall in different bank groups).
+constexpr int kEncCodeHalo = 16;
+constexpr int kEncCodeRows = 128 + kEncCodeHalo + 1;
+
+struct CodecInput {
+  const int8_t* codes;       // [Lr][T][d]
+  const float* scales;       // [Lr][T]
+  const int32_t* cu_seqlens;   // [n_req + 1]
+  int32_t* anchor;           // [T] workspace: token of each token's group anchor, -1 for a
+                             // token in no request (written by the prepare kernel)
+  int32_t n_req, group_tokens, n_layers_total;
+  float bins[3];
+  int32_t exact_products;    // every code times every bin is exact in binary32
+};
+
 struct PrepareParams {
   // A0: placement
   const int32_t* cu_seqlens;
@@ -123,6 +154,8 @@ struct PrepareParams {
   float* mean;   // [Lr][T] (LayerNorm only)
   uint32_t* err;
   int32_t slot_blocks;  // leading blocks of the grid that do placement
+  int32_t layer_begin;  // model layer of hidden layer 0 (codec bins)
+  CodecInput enc;       // codes != nullptr: statistics of the decoded rows
 };
 
 struct ProjectParams {
@@ -168,6 +201,13 @@ int project_pair_clusters(int dtype);
 cudaError_t launch_project_swap(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w5,
                                 const ProjectParams& p, int grid, cudaStream_t s);
 int project_swap_clusters(int dtype);
+// Token-row CTA pairs whose A operand is decoded from the codec's int8 codes
+// in shared memory: tmap_c is the codes' 3-D map (d, T, Lr) with 128-row
+// boxes, tmap_w the pair's half-tile weight map.  grid is even.
+cudaError_t launch_project_enc(const CUtensorMap& tmap_c, const CUtensorMap& tmap_w,
+                               const ProjectParams& p, const CodecInput& e, int grid,
+                               cudaStream_t s);
+int project_enc_clusters(int dtype);
 cudaError_t launch_pack_weights(const void* w_k, const void* w_v, const void* gamma, void* dst,
                                 int d_kv, int d, int dtype, cudaStream_t s);
 cudaError_t launch_column_constants(const void* w_packed, const void* w_k, const void* w_v,

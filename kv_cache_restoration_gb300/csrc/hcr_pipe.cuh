@@ -64,6 +64,25 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   }
 }
 
+// wait_phase whose probes may sleep up to sleep_ns each until the phase
+// completes (same bound, same abort and diagnostics).
+__device__ __forceinline__ bool wait_phase_sleep(uint32_t bar, uint32_t parity,
+                                                 volatile int32_t* abort, const ProjectParams& p,
+                                                 uint32_t code, uint32_t a, uint32_t b,
+                                                 uint32_t sleep_ns) {
+  if (ptx::mbar_try_wait_sleep(bar, parity, sleep_ns)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait_sleep(bar, parity, sleep_ns)) return true;
+    if (*abort) return false;
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      record_timeout(p, code, a, b, parity);
+      return false;
+    }
+  }
+}
+
 // Bounded wait used only while shutting down after an abort.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = ptx::globaltimer_ns();

@@ -13,7 +13,11 @@
 //     deviations from that mean.  The hidden states are the layer inputs the
 //     HCache episode ("Fast State Restoration for Evicted LLM KV Caches",
 //     cue 14) restores from; applying the input norm is this library's
-//     reading of its K = W_k H shorthand for pre-norm models.
+//     reading of its K = W_k H shorthand for pre-norm models.  With the
+//     codec's encoded form as input the warp decodes the row (its codes, its
+//     group anchor's codes and scale) into the values hcr_decode_hidden would
+//     store and reduces those, and placement also records each token's group
+//     anchor for the projection.
 //
 // pack_kernel and column_constants_kernel run once in hcr_create: the packed
 // weight W'[j][i] = W[j][i] * gamma[i] (W = [W_k; W_v]) rounded once to the
@@ -22,6 +26,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "hcr_decode.cuh"
 #include "hcr_internal.h"
 
 namespace hcr {
@@ -104,20 +109,78 @@ __device__ void place_token(const PrepareParams& p, int t) {
   if (bad) atomicOr(p.err, bad);
   p.slot[t] = slot;
   p.pos[t] = pos;
+  if (p.enc.anchor) {
+    const int g = p.enc.group_tokens;
+    p.enc.anchor[t] = (c0 >= 0 && c0 <= t && t < c1) ? c0 + (t - c0) / g * g : -1;
+  }
 }
 
-template <int DT>
-__device__ void row_stats(const PrepareParams& p, int64_t row, int lane) {
+// The storage-type values of one hidden row, 8 at a time (vector v holds
+// elements 8v .. 8v+7): read as stored, or decoded from the codec's codes
+// exactly as hcr_decode_hidden writes them.
+template <int DT, bool ENC>
+struct RowSource {
+  const uint4* hv;        // stored row
+  const uint2* own;       // encoded: the row's codes
+  const uint2* anchor;    // encoded: its group anchor's codes
+  float s, b;             // encoded: anchor scale, layer bin
+  bool is_anchor;
+
+  __device__ __forceinline__ uint4 operator()(int v) const {
+    if constexpr (!ENC) {
+      return __ldg(hv + v);
+    } else {
+      float2 q[4], a[4];
+      dec::codes_to_float(__ldg(anchor + v), q);
+      dec::anchor8(q, s, a);
+      if (is_anchor) return dec::narrow8<DT>(a);
+      float2 c[4], y[4];
+      dec::codes_to_float(__ldg(own + v), c);
+      dec::delta8(a, c, b, y);
+      return dec::narrow8<DT>(y);
+    }
+  }
+};
+
+template <int DT, bool ENC>
+__device__ RowSource<DT, ENC> row_source(const PrepareParams& p, int64_t row) {
+  RowSource<DT, ENC> src{};
   const int d = p.d_model;
-  const uint16_t* h = reinterpret_cast<const uint16_t*>(p.hidden) + row * int64_t(d);
-  const uint4* hv = reinterpret_cast<const uint4*>(h);
+  if constexpr (!ENC) {
+    src.hv = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.hidden) +
+                                            row * int64_t(d));
+  } else {
+    const CodecInput& e = p.enc;
+    const int li = int(row / p.n_tokens);
+    const int t = int(row - int64_t(li) * p.n_tokens);
+    int r, c0, c1;
+    int64_t arow = row;   // a token in no request decodes as zeros (and is flagged by placement)
+    src.s = 0.f;
+    src.is_anchor = true;
+    if (dec::request_of(e.cu_seqlens, e.n_req, t, &r, &c0, &c1)) {
+      const int a = c0 + (t - c0) / e.group_tokens * e.group_tokens;
+      arow = int64_t(li) * p.n_tokens + a;
+      src.s = __ldg(e.scales + arow);
+      src.is_anchor = a == t;
+    }
+    src.own = reinterpret_cast<const uint2*>(e.codes + row * int64_t(d));
+    src.anchor = reinterpret_cast<const uint2*>(e.codes + arow * int64_t(d));
+    src.b = dec::layer_bin(e, p.layer_begin + li);
+  }
+  return src;
+}
+
+template <int DT, bool ENC>
+__device__ void row_stats(const PrepareParams& p, int64_t row, int lane) {
+  const RowSource<DT, ENC> src = row_source<DT, ENC>(p, row);
+  const int d = p.d_model;
   const int nvec = d >> 3;
   const float inv_d = 1.0f / float(d);
   if (!p.layer_norm) {
     float s2 = 0.f;
 #pragma unroll 4
     for (int v = lane; v < nvec; v += 32) {
-      const uint4 q = __ldg(hv + v);
+      const uint4 q = src(v);
       const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -135,11 +198,11 @@ __device__ void row_stats(const PrepareParams& p, int64_t row, int lane) {
   // then the sum of squared deviations from that mean.  The second pass reads
   // the row again from L1/L2.  A one-pass sum(x^2) - mean^2 cancels when
   // |mean| or an outlier channel is large against the spread.
-  const float shift = to_float<DT>(__ldg(h));
+  const float shift = to_float2<DT>(src(0).x).x;
   float s1 = 0.f;
 #pragma unroll 4
   for (int v = lane; v < nvec; v += 32) {
-    const uint4 q = __ldg(hv + v);
+    const uint4 q = src(v);
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -152,7 +215,7 @@ __device__ void row_stats(const PrepareParams& p, int64_t row, int lane) {
   float s2 = 0.f;
 #pragma unroll 4
   for (int v = lane; v < nvec; v += 32) {
-    const uint4 q = __ldg(hv + v);
+    const uint4 q = src(v);
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -169,7 +232,7 @@ __device__ void row_stats(const PrepareParams& p, int64_t row, int lane) {
   }
 }
 
-template <int DT>
+template <int DT, bool ENC>
 __global__ void __launch_bounds__(kPrepareThreads) prepare_kernel(const PrepareParams p) {
   if (int(blockIdx.x) < p.slot_blocks) {
     const int t = blockIdx.x * kPrepareThreads + threadIdx.x;
@@ -185,7 +248,7 @@ __global__ void __launch_bounds__(kPrepareThreads) prepare_kernel(const PrepareP
   const int64_t row =
       int64_t(blockIdx.x - p.slot_blocks) * warps + (threadIdx.x >> 5);
   if (row >= int64_t(p.n_layers) * p.n_tokens) return;
-  row_stats<DT>(p, row, threadIdx.x & 31);
+  row_stats<DT, ENC>(p, row, threadIdx.x & 31);
 }
 
 // W'[j][i] = round(W[j][i] * gamma[i]); rows j < d_kv from w_k, the rest from w_v.
@@ -247,10 +310,18 @@ cudaError_t launch_prepare(const PrepareParams& p0, cudaStream_t s) {
   const int64_t grid = p.slot_blocks + stat_blocks;
   if (grid <= 0) return cudaSuccess;
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
-  if (p.dtype == HCR_DTYPE_BF16)
-    prepare_kernel<HCR_DTYPE_BF16><<<unsigned(grid), kPrepareThreads, 0, s>>>(p);
-  else
-    prepare_kernel<HCR_DTYPE_FP16><<<unsigned(grid), kPrepareThreads, 0, s>>>(p);
+  const bool enc = p.enc.codes != nullptr;
+  if (p.dtype == HCR_DTYPE_BF16) {
+    if (enc)
+      prepare_kernel<HCR_DTYPE_BF16, true><<<unsigned(grid), kPrepareThreads, 0, s>>>(p);
+    else
+      prepare_kernel<HCR_DTYPE_BF16, false><<<unsigned(grid), kPrepareThreads, 0, s>>>(p);
+  } else {
+    if (enc)
+      prepare_kernel<HCR_DTYPE_FP16, true><<<unsigned(grid), kPrepareThreads, 0, s>>>(p);
+    else
+      prepare_kernel<HCR_DTYPE_FP16, false><<<unsigned(grid), kPrepareThreads, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -187,6 +187,44 @@ class Restorer:
                             self._stream(stream))
         return out
 
+    def encoded_workspace(self, n_tokens: int, n_layers: int, device) -> torch.Tensor:
+        need = B.hcr_encoded_workspace_bytes(self.handle, n_tokens, n_layers)
+        ws = getattr(self, "_enc_ws", None)
+        if ws is None or ws.numel() < need or ws.device != torch.device(device):
+            self._enc_ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        return self._enc_ws
+
+    def restore_encoded(self, codes, scales, layer_begin, layer_end, cu_seqlens, start_pos,
+                        block_table, k_cache, v_cache, num_blocks, block_size,
+                        bins=(0.5, 1.0, 1.5), group_tokens: int = 10, layer_stride_elems=0,
+                        stream=None, workspace=None, check: bool = True) -> int:
+        """Restore from the codec's form in device memory (codes int8
+        [Lr][T][d], scales float32 [Lr][T]), decoded inside the kernels."""
+        dt = self.torch_dtype
+        for name, t, want in (("codes", codes, torch.int8), ("scales", scales, torch.float32),
+                              ("k_cache", k_cache, dt), ("v_cache", v_cache, dt),
+                              ("cu_seqlens", cu_seqlens, torch.int32),
+                              ("start_pos", start_pos, torch.int32),
+                              ("block_table", block_table, torch.int32)):
+            if not isinstance(t, torch.Tensor) or not t.is_cuda:
+                raise ValueError(f"{name} must be a CUDA tensor")
+            if t.dtype != want:
+                raise TypeError(f"{name} must be {want}, got {t.dtype}")
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+        if codes.dim() != 3 or codes.shape[-1] != self.dims.d_model:
+            raise ValueError(f"codes must be [layers][tokens][{self.dims.d_model}]")
+        T = int(codes.shape[-2])
+        nl = layer_end - layer_begin
+        if workspace is None:
+            workspace = self.encoded_workspace(T, max(nl, 1), codes.device)
+        return B.hcr_restore_encoded(
+            self.handle, B.codec_params(bins, group_tokens), codes, scales, layer_begin,
+            layer_end, int(start_pos.numel()), T, cu_seqlens, start_pos, block_table,
+            int(block_table.shape[-1]), k_cache, v_cache,
+            B.hcr_cache_layout(num_blocks, block_size, layer_stride_elems), workspace,
+            workspace.numel(), self._stream(stream), check=check)
+
     def plan_split(self, n_tokens: int, layers_per_chunk: int = 4, reps: int = 5, stream=None):
         """Profiles the per-layer costs on this GPU and returns (costs, split)."""
         costs = B.hcr_profile_layer_costs(self.handle, n_tokens, layers_per_chunk, reps,

@@ -7,16 +7,21 @@
 // CacheGen compresses KV caches (CacheGen review, section 核心方法: groups of
 // 10 tokens, an 8-bit anchor per group, the other tokens as quantised deltas
 // from it).  Here the restore reads that form directly: TMA brings each
-// k-block's int8 codes (8 KB for a CTA's 128 rows, half the bytes of the
-// hidden states) into shared memory, and converter warps write the bf16/fp16
-// A stage the MMA reads, in the 128-byte-swizzled K-major layout a TMA load
-// would have produced:
+// k-block's int8 codes (half the bytes of the hidden states) into shared
+// memory, and converter warps write the bf16/fp16 A stage the MMA reads, in
+// the 128-byte-swizzled K-major layout a TMA load would have produced:
 //     anchor row:  q * s                     (its codes, its scale)
 //     other rows:  q_anchor * s + c * b       (its codes c, the layer's bin b)
 // each one binary32 operation, then one rounding to the storage type, so the
 // operand, and therefore every cache element, is bit-identical to restoring
 // from hcr_decode_hidden's output.  The norm statistics come from the prepare
 // kernel decoding the same rows; the epilogue is the token-row kernel's.
+//
+// On GB300 this restore is slower than the decode kernel followed by the
+// token-row kernel (8.3 against 5.8 ms for the Llama2-7B-shaped step): every A
+// tile is decoded again for each of the 32 n-tiles, and the k-block's period
+// follows the converter warps' latency on it.  The layer-pipelined encoded
+// restore therefore decodes first.
 //
 // Warp roles (480 threads, one CTA per SM, clusters of two):
 //   warp 0       one lane loads the pair's weight half-tiles (TMA, completion

@@ -206,3 +206,33 @@ def test_stalled_encoded_pipeline_times_out_and_context_survives(cuda_device):
     _restore_encoded(again, codes, scales, params)
     for c in ("k_cache", "v_cache"):
         assert torch.equal(getattr(again, c).view(torch.int16), getattr(ref, c).view(torch.int16))
+
+
+# One layer of each benchmark workload at full size, one per layer third (bins
+# 0.5 / 1.0 / 1.5): the 13B shape with shuffled blocks, OPT-30B (fp16,
+# LayerNorm, biases, d = 7168), and the ragged batch of 64 requests, whose
+# anchor groups restart at every request boundary.
+FULL = [("llama2-13b", 20), ("opt-30b", 47), ("ragged-7b", 0)]
+
+
+@pytest.mark.parametrize("name,layer", FULL, ids=[n for n, _ in FULL])
+def test_encoded_restore_full_size_layer(cuda_device, name, layer):
+    w = C.get(name)
+    params = ((0.5, 1.0, 1.5), 10)
+    ref = Hn.make_case(w, cuda_device, layer, layer + 1, gen_device=cuda_device)
+    codes, scales, dec = _encode_decode(ref, params)
+    ref.hidden = dec
+    Hn.run(ref)
+    assert ref.status == 0
+    k_ref, v_ref = ref.k_cache, ref.v_cache
+    fused = Hn.make_case(w, cuda_device, layer, layer + 1, params=ref.params,
+                         restorer=ref.restorer, gen_device=cuda_device)
+    del ref
+    fused.hidden = None
+    torch.cuda.empty_cache()
+    _restore_encoded(fused, codes, scales, params)
+    assert torch.equal(fused.k_cache.view(torch.int16), k_ref.view(torch.int16))
+    assert torch.equal(fused.v_cache.view(torch.int16), v_ref.view(torch.int16))
+    del k_ref, v_ref
+    fused.hidden = dec
+    Hn.compare(fused, rows=Hn.sample_rows(w, 1 / 256), check_sentinel=False)

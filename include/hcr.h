@@ -212,7 +212,15 @@ hcr_status hcr_restore_project(hcr_handle* h, const void* hidden, int32_t layer_
  *              decides the ring: min(8, staging_bytes / chunk bytes) slots,
  *              at least one (one slot restores correctly but serialises).
  * workspace:   as hcr_restore, sized for one chunk:
- *              hcr_workspace_bytes(h, n_tokens, layers_per_chunk).
+ *              hcr_workspace_bytes(h, n_tokens, layers_per_chunk).  Given
+ *              statistics room for every slot's chunk,
+ *              hcr_workspace_bytes(h, n_tokens, slots * layers_per_chunk),
+ *              the slot map is computed once and each chunk's norm
+ *              statistics on a second stream the handle owns as soon as
+ *              the chunk lands, so `stream` runs only the projections; the
+ *              caches are the same bits either way.  The same holds for
+ *              hcr_restore_streamed_chunks, hcr_restore_streamed_split
+ *              (hidden-state groups) and hcr_restore_streamed_encoded.
  * Every other argument is as in hcr_restore (k_cache and v_cache are the
  * base of layer layer_begin).  Returns after enqueueing; the restore is
  * complete when `stream` reaches this point.  Calls through one handle are

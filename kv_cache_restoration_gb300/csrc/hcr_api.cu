@@ -133,6 +133,12 @@ hcr_status validate_dims(const hcr_model_dims* d) {
   return HCR_OK;
 }
 
+#define HCR_RESTORE_ARGS_IN                                                                      \
+  RestoreArgs a{hidden,     layer_begin, layer_end,          n_req,   n_tokens,                  \
+                cu_seqlens, start_pos,   block_table,        max_blocks_per_req,                 \
+                k_cache,    v_cache,     layout,             workspace, workspace_bytes,         \
+                static_cast<cudaStream_t>(stream)}
+
 struct RestoreArgs {
   const void* hidden;
   int32_t layer_begin, layer_end, n_req, n_tokens;
@@ -143,6 +149,10 @@ struct RestoreArgs {
   void* workspace;
   size_t workspace_bytes;
   cudaStream_t stream;
+  // Statistics of the call's rows, [layer][token], when they do not live in
+  // the workspace (the layer-pipelined restores keep one set per staging slot)
+  const float* rstd = nullptr;
+  const float* mean = nullptr;
 };
 
 // Returns HCR_OK with *empty set when there is nothing to do.  `stats` says
@@ -197,7 +207,8 @@ hcr_status validate_restore(const hcr_handle* h, const RestoreArgs& a, bool* emp
 // enc: the statistics of the rows decoded from the codec's form, and each
 // token's group anchor for the projection (a.hidden is then unused).
 hcr_status do_prepare(hcr_handle* h, const RestoreArgs& a, bool stats = true,
-                      const CodecInput* enc = nullptr) {
+                      const CodecInput* enc = nullptr, float* stats_rstd = nullptr,
+                      float* stats_mean = nullptr) {
   NvtxRange range("hcr.prepare");
   const Handle& H = h->impl;
   const hcr_model_dims& d = H.dims;
@@ -228,6 +239,11 @@ hcr_status do_prepare(hcr_handle* h, const RestoreArgs& a, bool stats = true,
   p.mean = p.layer_norm ? reinterpret_cast<float*>(ws + w.mean_off) : nullptr;
   p.err = H.err;
   p.layer_begin = a.layer_begin;
+  if (stats_rstd) {   // statistics only, into the given arrays
+    p.skip_placement = 1;
+    p.rstd = stats_rstd;
+    p.mean = p.layer_norm ? stats_mean : nullptr;
+  }
   if (enc) {
     p.enc = *enc;
     p.enc.anchor = reinterpret_cast<int32_t*>(ws + w.anchor_off);
@@ -372,8 +388,9 @@ hcr_status do_project_swap(hcr_handle* h, const RestoreArgs& a) {
   p.dtype = d.dtype;
   p.slot = reinterpret_cast<const int64_t*>(ws + w.slot_off);
   p.pos = reinterpret_cast<const int32_t*>(ws + w.pos_off);
-  p.rstd = reinterpret_cast<const float*>(ws + w.rstd_off);
-  p.mean = p.layer_norm ? reinterpret_cast<const float*>(ws + w.mean_off) : nullptr;
+  p.rstd = a.rstd ? a.rstd : reinterpret_cast<const float*>(ws + w.rstd_off);
+  p.mean = !p.layer_norm ? nullptr
+                         : (a.mean ? a.mean : reinterpret_cast<const float*>(ws + w.mean_off));
   p.col_sum = H.col_sum ? H.col_sum + int64_t(a.layer_begin) * 2 * d_kv : nullptr;
   p.col_bias = H.col_bias ? H.col_bias + int64_t(a.layer_begin) * 2 * d_kv : nullptr;
   p.rope_tab = H.rope_tab;
@@ -420,8 +437,9 @@ ProjectParams token_row_params(const Handle& H, const RestoreArgs& a, bool pair,
   p.dtype = d.dtype;
   p.slot = reinterpret_cast<const int64_t*>(ws + w.slot_off);
   p.pos = reinterpret_cast<const int32_t*>(ws + w.pos_off);
-  p.rstd = reinterpret_cast<const float*>(ws + w.rstd_off);
-  p.mean = p.layer_norm ? reinterpret_cast<const float*>(ws + w.mean_off) : nullptr;
+  p.rstd = a.rstd ? a.rstd : reinterpret_cast<const float*>(ws + w.rstd_off);
+  p.mean = !p.layer_norm ? nullptr
+                         : (a.mean ? a.mean : reinterpret_cast<const float*>(ws + w.mean_off));
   p.col_sum = H.col_sum ? H.col_sum + int64_t(a.layer_begin) * 2 * d_kv : nullptr;
   p.col_bias = H.col_bias ? H.col_bias + int64_t(a.layer_begin) * 2 * d_kv : nullptr;
   p.rope_tab = H.rope_tab;
@@ -507,6 +525,55 @@ hcr_status do_project_enc(hcr_handle* h, const RestoreArgs& a, const CodecInput&
   if (err != cudaSuccess) return cuda_fail(err, "project launch (encoded input)");
   return HCR_OK;
 }
+
+}  // namespace
+
+// Pieces of hcr_restore for the layer-pipelined restores (hcr_streamed.cu).
+hcr_status pipeline_placement(hcr_handle* h, const void* staging, int32_t layer_begin,
+                              int32_t layer_end, int32_t n_req, int32_t n_tokens,
+                              const int32_t* cu_seqlens, const int32_t* start_pos,
+                              const int32_t* block_table, int32_t max_blocks_per_req,
+                              void* k_cache, void* v_cache, const hcr_cache_layout* layout,
+                              void* workspace, size_t workspace_bytes, int32_t stats_layers,
+                              void* stream, bool* ok) {
+  *ok = false;
+  const void* hidden = staging;
+  HCR_RESTORE_ARGS_IN;
+  bool empty = false;
+  hcr_status st = validate_restore(h, a, &empty, /*stats=*/false, "staging");
+  if (st != HCR_OK || empty) return st;
+  const WorkspaceLayout w = workspace_layout(n_tokens, stats_layers,
+                                             h->impl.dims.norm == HCR_NORM_LAYER);
+  if (workspace_bytes < w.total) return HCR_OK;   // no room: the caller restores group by group
+  *ok = true;
+  return do_prepare(h, a, /*stats=*/false);
+}
+
+hcr_status pipeline_stats(hcr_handle* h, const void* hidden, int32_t layer_begin,
+                          int32_t layer_end, int32_t n_req, int32_t n_tokens,
+                          const int32_t* cu_seqlens, const int32_t* start_pos,
+                          const int32_t* block_table, int32_t max_blocks_per_req,
+                          void* k_cache, void* v_cache, const hcr_cache_layout* layout,
+                          void* workspace, size_t workspace_bytes, float* rstd, float* mean,
+                          void* stream) {
+  HCR_RESTORE_ARGS_IN;
+  return do_prepare(h, a, true, nullptr, rstd, mean);
+}
+
+hcr_status pipeline_project(hcr_handle* h, const void* hidden, int32_t layer_begin,
+                            int32_t layer_end, int32_t n_req, int32_t n_tokens,
+                            const int32_t* cu_seqlens, const int32_t* start_pos,
+                            const int32_t* block_table, int32_t max_blocks_per_req,
+                            void* k_cache, void* v_cache, const hcr_cache_layout* layout,
+                            void* workspace, size_t workspace_bytes, const float* rstd,
+                            const float* mean, void* stream) {
+  HCR_RESTORE_ARGS_IN;
+  a.rstd = rstd;
+  a.mean = mean;
+  return do_project(h, a);
+}
+
+namespace {
 
 void free_handle(Handle& H) {
   release_streamed(H);

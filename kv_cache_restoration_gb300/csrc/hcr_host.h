@@ -71,6 +71,38 @@ cudaError_t launch_kv_rows(const KvRowsParams& p, bool to_cache, int num_sms, cu
 // names `what` when the device cannot address it.
 hcr_status device_view(const Handle& H, void* ptr, const char* what, void** out);
 
+// Pieces of hcr_restore for the layer-pipelined restores (hcr_streamed.cu);
+// arguments as in hcr_restore.
+//   pipeline_placement: checks a whole call's arguments (`staging` stands for
+//     the hidden rows) and, when the workspace also holds statistics for
+//     stats_layers layers (*ok), enqueues the slot map on `stream`.
+//   pipeline_stats: the norm statistics of hidden rows [layer_begin,
+//     layer_end) into rstd / mean ([layer][token]) on `stream` (the slot map
+//     is not touched).
+//   pipeline_project: the projection of those rows with the given statistics
+//     and the slot map already in the workspace.
+hcr_status pipeline_placement(hcr_handle* h, const void* staging, int32_t layer_begin,
+                              int32_t layer_end, int32_t n_req, int32_t n_tokens,
+                              const int32_t* cu_seqlens, const int32_t* start_pos,
+                              const int32_t* block_table, int32_t max_blocks_per_req,
+                              void* k_cache, void* v_cache, const hcr_cache_layout* layout,
+                              void* workspace, size_t workspace_bytes, int32_t stats_layers,
+                              void* stream, bool* ok);
+hcr_status pipeline_stats(hcr_handle* h, const void* hidden, int32_t layer_begin,
+                          int32_t layer_end, int32_t n_req, int32_t n_tokens,
+                          const int32_t* cu_seqlens, const int32_t* start_pos,
+                          const int32_t* block_table, int32_t max_blocks_per_req,
+                          void* k_cache, void* v_cache, const hcr_cache_layout* layout,
+                          void* workspace, size_t workspace_bytes, float* rstd, float* mean,
+                          void* stream);
+hcr_status pipeline_project(hcr_handle* h, const void* hidden, int32_t layer_begin,
+                            int32_t layer_end, int32_t n_req, int32_t n_tokens,
+                            const int32_t* cu_seqlens, const int32_t* start_pos,
+                            const int32_t* block_table, int32_t max_blocks_per_req,
+                            void* k_cache, void* v_cache, const hcr_cache_layout* layout,
+                            void* workspace, size_t workspace_bytes, const float* rstd,
+                            const float* mean, void* stream);
+
 // Host checks of a codec call (hcr_encode_hidden / hcr_decode_hidden); sets
 // *empty for a call with no work.
 hcr_status check_codec(const hcr_handle* h, const hcr_codec_params* cp, int32_t layer_begin,

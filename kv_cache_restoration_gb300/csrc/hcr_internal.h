@@ -154,6 +154,7 @@ struct PrepareParams {
   float* mean;   // [Lr][T] (LayerNorm only)
   uint32_t* err;
   int32_t slot_blocks;  // leading blocks of the grid that do placement
+  int32_t skip_placement;   // statistics only (the slot map is written elsewhere)
   int32_t layer_begin;  // model layer of hidden layer 0 (codec bins)
   CodecInput enc;       // codes != nullptr: statistics of the decoded rows
 };

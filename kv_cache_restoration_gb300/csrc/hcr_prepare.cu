@@ -304,7 +304,7 @@ __global__ void column_constants_kernel(const uint16_t* __restrict__ w_packed,
 
 cudaError_t launch_prepare(const PrepareParams& p0, cudaStream_t s) {
   PrepareParams p = p0;
-  p.slot_blocks = (p.n_tokens + kPrepareThreads - 1) / kPrepareThreads;
+  p.slot_blocks = p.skip_placement ? 0 : (p.n_tokens + kPrepareThreads - 1) / kPrepareThreads;
   const int64_t rows = int64_t(p.n_layers) * p.n_tokens;
   const int64_t stat_blocks = (rows + kPrepareThreads / 32 - 1) / (kPrepareThreads / 32);
   const int64_t grid = p.slot_blocks + stat_blocks;

@@ -103,12 +103,6 @@ hcr_status copy_status(cudaError_t e) {
   return set_last_error(HCR_ERR_CUDA, "host copy: %s", cudaGetErrorString(e));
 }
 
-// Enqueues an item's GPU work on the caller's stream once its copy has
-// landed in `src`: by default hcr_restore (hidden states) or hcr_load_kv
-// (K/V); `lb` is the item's first model layer, kc/vc its cache bases.
-using ProcessFn =
-    std::function<hcr_status(const Item& it, void* src, int32_t lb, void* kc, void* vc)>;
-
 hcr_status run_pipeline(hcr_handle* h, const std::vector<Item>& items, size_t slot_bytes,
                         int32_t layer_begin, int32_t n_req, int32_t n_tokens,
                         const int32_t* cu_seqlens, const int32_t* start_pos,
@@ -116,7 +110,7 @@ hcr_status run_pipeline(hcr_handle* h, const std::vector<Item>& items, size_t sl
                         void* v_cache, const hcr_cache_layout* layout, void* staging,
                         size_t staging_bytes, size_t workspace_need, void* workspace,
                         size_t workspace_bytes, void* stream, const CopyFn& copy_item,
-                        const ProcessFn* process = nullptr, const SideFn* side = nullptr) {
+                        const SideFn* side = nullptr, size_t hidden_offset = 0) {
   NvtxRange range("hcr.streamed_pipeline");
   const hcr_model_dims& d = h->impl.dims;
   if (!layout) return set_last_error(HCR_ERR_INVALID_ARG, "layout is NULL");
@@ -149,6 +143,29 @@ hcr_status run_pipeline(hcr_handle* h, const std::vector<Item>& items, size_t sl
   if ((e = cudaEventRecord(r->start, s)) != cudaSuccess) return cuda_err(e, "event record");
   if ((e = cudaStreamWaitEvent(r->copy, r->start, 0)) != cudaSuccess)
     return cuda_err(e, "stream wait");
+  // Overlapped statistics: when the workspace has room for one group's norm
+  // statistics per staging slot, the slot map is computed once here, each
+  // hidden-state group's statistics on the side stream as soon as the group
+  // has landed (and been decoded), and the caller's stream only projects.
+  // The statistics' read of the group's rows then runs under the previous
+  // group's projection instead of before its own.  Otherwise every group is
+  // restored with hcr_restore.
+  int32_t max_nl = 0, extent = 0;
+  for (const Item& it : items) {
+    if (!it.kv) max_nl = std::max(max_nl, it.nl);
+    extent = std::max(extent, it.l0 + it.nl);
+  }
+  bool overlap = false;
+  if (max_nl > 0 &&
+      (st = pipeline_placement(h, staging, layer_begin, layer_begin + extent, n_req, n_tokens,
+                               cu_seqlens, start_pos, block_table, max_blocks_per_req, k_cache,
+                               v_cache, layout, workspace, workspace_bytes, slots * max_nl,
+                               stream, &overlap)) != HCR_OK)
+    return st;
+  const WorkspaceLayout wl =
+      workspace_layout(n_tokens, int64_t(slots) * max_nl, d.norm == HCR_NORM_LAYER);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t slot_stats = size_t(max_nl) * size_t(n_tokens);   // floats per slot
   uint8_t* ring = static_cast<uint8_t*>(staging);
   for (size_t c = 0; c < items.size(); ++c) {
     const Item& it = items[c];
@@ -161,13 +178,27 @@ hcr_status run_pipeline(hcr_handle* h, const std::vector<Item>& items, size_t sl
       NvtxRange copy_range(it.kv ? "hcr.copy_kv_group" : "hcr.copy_hidden_group");
       if ((st = copy_item(it, dst, r->copy)) != HCR_OK) return st;
     }
+    const int32_t lb = layer_begin + it.l0;
+    uint8_t* rows = static_cast<uint8_t*>(dst) + hidden_offset;   // the group's hidden rows
+    const bool own_stats = overlap && !it.kv;
+    float* rstd = own_stats
+                      ? reinterpret_cast<float*>(ws + wl.rstd_off) + size_t(slot) * slot_stats
+                      : nullptr;
+    float* mean = own_stats && d.norm == HCR_NORM_LAYER
+                      ? reinterpret_cast<float*>(ws + wl.mean_off) + size_t(slot) * slot_stats
+                      : nullptr;
     cudaStream_t ready = r->copy;   // where the item is ready for processing
-    if (side) {
+    if ((side && !it.kv) || own_stats) {
       if ((e = cudaEventRecord(r->landed[slot], r->copy)) != cudaSuccess)
         return cuda_err(e, "event record");
       if ((e = cudaStreamWaitEvent(r->side, r->landed[slot], 0)) != cudaSuccess)
         return cuda_err(e, "stream wait");
-      if ((st = (*side)(it, dst, r->side)) != HCR_OK) return st;
+      if (side && !it.kv && (st = (*side)(it, dst, r->side)) != HCR_OK) return st;
+      if (own_stats &&
+          (st = pipeline_stats(h, rows, lb, lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos,
+                               block_table, max_blocks_per_req, k_cache, v_cache, layout,
+                               workspace, workspace_bytes, rstd, mean, r->side)) != HCR_OK)
+        return st;
       ready = r->side;
     }
     if ((e = cudaEventRecord(r->copied[slot], ready)) != cudaSuccess)
@@ -176,16 +207,18 @@ hcr_status run_pipeline(hcr_handle* h, const std::vector<Item>& items, size_t sl
       return cuda_err(e, "stream wait");
     auto* kc = static_cast<uint16_t*>(k_cache) + int64_t(it.l0) * stride;
     auto* vc = static_cast<uint16_t*>(v_cache) + int64_t(it.l0) * stride;
-    const int32_t lb = layer_begin + it.l0;
-    if (process)
-      st = (*process)(it, dst, lb, kc, vc);
+    if (it.kv)
+      st = hcr_load_kv(h, dst, lb, lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos,
+                       block_table, max_blocks_per_req, kc, vc, layout, workspace,
+                       workspace_bytes, stream);
+    else if (own_stats)
+      st = pipeline_project(h, rows, lb, lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos,
+                            block_table, max_blocks_per_req, kc, vc, layout, workspace,
+                            workspace_bytes, rstd, mean, stream);
     else
-      st = it.kv ? hcr_load_kv(h, dst, lb, lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos,
-                               block_table, max_blocks_per_req, kc, vc, layout, workspace,
-                               workspace_bytes, stream)
-                 : hcr_restore(h, dst, lb, lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos,
-                               block_table, max_blocks_per_req, kc, vc, layout, workspace,
-                               workspace_bytes, stream);
+      st = hcr_restore(h, rows, lb, lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos,
+                       block_table, max_blocks_per_req, kc, vc, layout, workspace,
+                       workspace_bytes, stream);
     if (st != HCR_OK) return st;
     if ((e = cudaEventRecord(r->done[slot], s)) != cudaSuccess)
       return cuda_err(e, "event record");
@@ -456,12 +489,6 @@ extern "C" hcr_status hcr_restore_streamed_encoded(
     return hcr_decode_hidden(h, params, slot, slot + codes_bytes, lb, lb + it.nl, n_req,
                              n_tokens, cu_seqlens, slot + codes_bytes + scales_bytes, side);
   };
-  const ProcessFn restore_decoded = [&](const Item& it, void* src, int32_t lb, void* kc,
-                                        void* vc) {
-    return hcr_restore(h, static_cast<uint8_t*>(src) + codes_bytes + scales_bytes, lb,
-                       lb + it.nl, n_req, n_tokens, cu_seqlens, start_pos, block_table,
-                       max_blocks_per_req, kc, vc, layout, workspace, workspace_bytes, stream);
-  };
   return run_pipeline(
       h, items, slot_bytes, layer_begin, n_req, n_tokens, cu_seqlens, start_pos, block_table,
       max_blocks_per_req, k_cache, v_cache, layout, staging, staging_bytes,
@@ -475,5 +502,5 @@ extern "C" hcr_status hcr_restore_streamed_encoded(
                               size_t(it.nl) * T * 4, cudaMemcpyHostToDevice, copy);
         return copy_status(e);
       },
-      &restore_decoded, &decode);
+      &decode, codes_bytes + scales_bytes);
 }

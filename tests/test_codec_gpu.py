@@ -119,7 +119,7 @@ def test_codec_rejects_bad_params(cuda_device):
     assert not codes.any()
 
 
-def _streamed_encoded(case, params, codes_host, scales_host, chunk, slots):
+def _streamed_encoded(case, params, codes_host, scales_host, chunk, slots, overlap=False):
     from kv_cache_restoration_gb300 import binding as B
     lay = case.layout
     T, d = case.w.n_tokens, case.w.shape.d_model
@@ -128,8 +128,9 @@ def _streamed_encoded(case, params, codes_host, scales_host, chunk, slots):
     nbytes = B.encoded_staging_bytes(T, d, c, slots)
     dev = case.k_cache.device
     staging = torch.empty(nbytes + 256, dtype=torch.uint8, device=dev)
-    ws = torch.empty(B.hcr_workspace_bytes(case.restorer.handle, T, c) + 256, dtype=torch.uint8,
-                     device=dev)
+    ws_layers = c * (min(slots, 8) if overlap else 1)   # overlap: statistics per slot
+    ws = torch.empty(B.hcr_workspace_bytes(case.restorer.handle, T, ws_layers) + 256,
+                     dtype=torch.uint8, device=dev)
     st = B.hcr_restore_streamed_encoded(
         case.restorer.handle, params, codes_host, scales_host, case.layer_begin, case.layer_end,
         int(case.start.numel()), T, case.cu, case.start, case.table, lay.max_blocks,
@@ -148,13 +149,14 @@ def _reference_from_decoded(w, device, params, layer_begin=0, layer_end=None, ge
     return src, codes.cpu().pin_memory(), scales.cpu().pin_memory()
 
 
+@pytest.mark.parametrize("overlap", [False, True], ids=["in-order", "side-stream-stats"])
 @pytest.mark.parametrize("chunk,slots", [(1, 2), (2, 3), (4, 1), (6, 2)])
-def test_streamed_encoded_matches_restore_of_decoded(cuda_device, chunk, slots):
+def test_streamed_encoded_matches_restore_of_decoded(cuda_device, chunk, slots, overlap):
     from kv_cache_restoration_gb300 import binding as B
     params = B.codec_params()
     ref, codes_h, scales_h = _reference_from_decoded(W, cuda_device, params)
     case = Hn.make_case(W, cuda_device, params=ref.params, restorer=ref.restorer)
-    assert _streamed_encoded(case, params, codes_h, scales_h, chunk, slots) == 0
+    assert _streamed_encoded(case, params, codes_h, scales_h, chunk, slots, overlap) == 0
     assert case.restorer.check()[0] == 0
     for c in ("k_cache", "v_cache"):
         assert torch.equal(getattr(case, c).view(torch.int16), getattr(ref, c).view(torch.int16))
@@ -173,7 +175,7 @@ def test_streamed_encoded_layer_subrange_and_full_7b(cuda_device):
                                                      gen_device=cuda_device)
     case = Hn.make_case(w, cuda_device, params=ref.params, restorer=ref.restorer,
                         gen_device=cuda_device)
-    assert _streamed_encoded(case, params, codes_h, scales_h, 4, 3) == 0
+    assert _streamed_encoded(case, params, codes_h, scales_h, 4, 3, overlap=True) == 0
     for c in ("k_cache", "v_cache"):
         assert torch.equal(getattr(case, c).view(torch.int16), getattr(ref, c).view(torch.int16))
 

@@ -98,7 +98,8 @@ def test_save_then_load_round_trip_on_a_layer_subrange(cuda_device):
     assert torch.equal(fresh.v_cache.view(torch.int16), ref.v_cache[2:4].view(torch.int16))
 
 
-def _split_restore(case, hidden_host, kv_host, split, chunk, slots, check=False):
+def _split_restore(case, hidden_host, kv_host, split, chunk, slots, check=False,
+                   overlap=False):
     from kv_cache_restoration_gb300 import binding as B
     lay = case.layout
     s = case.w.shape
@@ -109,8 +110,10 @@ def _split_restore(case, hidden_host, kv_host, split, chunk, slots, check=False)
                      2 * T * s.n_kv_heads * s.head_dim * 2 if case.layer_end > split else 0)
     dev = case.k_cache.device
     staging = torch.empty(slots * slot_bytes + 256, dtype=torch.uint8, device=dev)
-    ws = torch.empty(B.hcr_workspace_bytes(case.restorer.handle, T, ch) + 256, dtype=torch.uint8,
-                     device=dev)
+    # overlap: statistics room for every slot's hidden-state group (side stream)
+    ws_layers = ch * (min(slots, 8) if overlap else 1)
+    ws = torch.empty(B.hcr_workspace_bytes(case.restorer.handle, T, ws_layers) + 256,
+                     dtype=torch.uint8, device=dev)
     st = B.hcr_restore_streamed_split(
         case.restorer.handle, hidden_host, kv_host, case.layer_begin, split, case.layer_end,
         int(case.start.numel()), T, case.cu, case.start, case.table, lay.max_blocks,
@@ -148,7 +151,8 @@ def test_streamed_split_matches_restore(cuda_device, split, chunk, slots):
     kv_host = _saved_kv_host(ref, split, 5)
     hidden_host = ref.hidden[:split].cpu().pin_memory() if split else None
     case = Hn.make_case(W, cuda_device, params=ref.params, restorer=ref.restorer)
-    assert _split_restore(case, hidden_host, kv_host, split, chunk, slots) == 0
+    overlap = slots > 2   # side-stream statistics for the 3-slot cases
+    assert _split_restore(case, hidden_host, kv_host, split, chunk, slots, overlap=overlap) == 0
     assert case.restorer.check()[0] == 0
     _same(case, ref)
 
@@ -170,7 +174,7 @@ def test_streamed_split_full_size_7b(cuda_device):
     hidden_host = ref.hidden[:28].cpu().pin_memory()
     case = Hn.make_case(w, cuda_device, params=ref.params, restorer=ref.restorer,
                         gen_device=cuda_device)
-    assert _split_restore(case, hidden_host, kv_host, 28, 4, 3) == 0
+    assert _split_restore(case, hidden_host, kv_host, 28, 4, 3, overlap=True) == 0
     _same(case, ref)
 
 

@@ -48,7 +48,7 @@ def _source(store, chunk_tokens, n, table_np, lay):
     return src
 
 
-def _restore_chunks(case, src, chunk, slots, check=False):
+def _restore_chunks(case, src, chunk, slots, check=False, overlap=False):
     from kv_cache_restoration_gb300 import binding as B
     lay = case.layout
     T, d = case.w.n_tokens, case.w.shape.d_model
@@ -56,7 +56,9 @@ def _restore_chunks(case, src, chunk, slots, check=False):
     chunk_bytes = min(chunk, nl) * T * d * 2
     dev = case.k_cache.device
     staging = torch.empty(slots * chunk_bytes + 256, dtype=torch.uint8, device=dev)
-    ws = torch.empty(B.hcr_workspace_bytes(case.restorer.handle, T, min(chunk, nl)) + 256,
+    # overlap: statistics room for every slot's group (computed on the side stream)
+    ws_layers = min(chunk, nl) * (min(slots, 8) if overlap else 1)
+    ws = torch.empty(B.hcr_workspace_bytes(case.restorer.handle, T, ws_layers) + 256,
                      dtype=torch.uint8, device=dev)
     st = B.hcr_restore_streamed_chunks(
         case.restorer.handle, src, case.layer_begin, case.layer_end, int(case.start.numel()), T,
@@ -87,7 +89,8 @@ def test_restore_from_chunk_store_matches_restore(cuda_device, chunk_tokens, chu
     store, table_np, n = _save_to_host(ref, chunk_tokens, order)
     case = Hn.make_case(W, cuda_device, params=ref.params, restorer=ref.restorer)
     src = _source(store, chunk_tokens, n, table_np, case.layout)
-    assert _restore_chunks(case, src, chunk, slots) == 0
+    overlap = chunk_tokens == 16   # one third of the cases with side-stream statistics
+    assert _restore_chunks(case, src, chunk, slots, overlap=overlap) == 0
     assert case.restorer.check()[0] == 0
     _same(case, ref)
 
@@ -107,7 +110,8 @@ def test_restore_from_chunk_store_full_size_7b(cuda_device):
     store, table_np, n = _save_to_host(ref, 64)
     case = Hn.make_case(w, cuda_device, params=ref.params, restorer=ref.restorer,
                         gen_device=cuda_device)
-    assert _restore_chunks(case, _source(store, 64, n, table_np, case.layout), 4, 3) == 0
+    assert _restore_chunks(case, _source(store, 64, n, table_np, case.layout), 4, 3,
+                           overlap=True) == 0
     _same(case, ref)
 
 

@@ -11,7 +11,9 @@ from workloads.configs import ModelShape, Workload
 pytestmark = pytest.mark.gpu
 
 
-def _streamed(case, chunk, slots, stream=None, pinned=True):
+def _streamed(case, chunk, slots, stream=None, pinned=True, overlap=False):
+    """overlap: a workspace with statistics room for every slot's group, so the
+    statistics run on the handle's side stream; otherwise room for one group."""
     from kv_cache_restoration_gb300 import binding as B
     lay = case.layout
     T, d = case.w.n_tokens, case.w.shape.d_model
@@ -21,7 +23,8 @@ def _streamed(case, chunk, slots, stream=None, pinned=True):
         host = host.pin_memory()
     chunk_bytes = min(chunk, nl) * T * d * 2
     staging = torch.empty(slots * chunk_bytes + 256, dtype=torch.uint8, device=case.hidden.device)
-    ws = torch.empty(B.hcr_workspace_bytes(case.restorer.handle, T, min(chunk, nl)) + 256,
+    ws_layers = min(chunk, nl) * (min(slots, 8) if overlap else 1)
+    ws = torch.empty(B.hcr_workspace_bytes(case.restorer.handle, T, ws_layers) + 256,
                      dtype=torch.uint8, device=case.hidden.device)
     st = B.hcr_restore_streamed(case.restorer.handle, host, case.layer_begin, case.layer_end,
                                 int(case.start.numel()), T, case.cu, case.start, case.table,
@@ -42,14 +45,29 @@ W4 = Workload("st4", ModelShape("st4", 5, 512, 4, 4, 128), (1, 200, 0, 77, 300),
               (0, 5, 9, 1000, 31), block_order="shuffled", spare_blocks=3)
 
 
+@pytest.mark.parametrize("overlap", [False, True], ids=["in-order", "side-stream-stats"])
 @pytest.mark.parametrize("chunk,slots", [(1, 2), (2, 2), (2, 3), (3, 1), (5, 8), (9, 2)])
-def test_streamed_matches_restore(cuda_device, chunk, slots):
+def test_streamed_matches_restore(cuda_device, chunk, slots, overlap):
     ref = Hn.run(Hn.make_case(W4, cuda_device))
     assert ref.status == 0
     case = Hn.make_case(W4, cuda_device, params=ref.params, restorer=ref.restorer)
-    assert _streamed(case, chunk, slots) == 0
+    assert _streamed(case, chunk, slots, overlap=overlap) == 0
     assert case.restorer.check()[0] == 0
     _same(case, ref)
+
+
+# LayerNorm (mean and rstd per row), fp16, biases
+WLN = Workload("stln", ModelShape("stln", 4, 384, 3, 3, 128, norm="ln", rope=False,
+                                  dtype="fp16", kv_bias=True), (250, 10), (0, 40))
+
+
+@pytest.mark.parametrize("overlap", [False, True], ids=["in-order", "side-stream-stats"])
+def test_streamed_layernorm(cuda_device, overlap):
+    ref = Hn.run(Hn.make_case(WLN, cuda_device))
+    case = Hn.make_case(WLN, cuda_device, params=ref.params, restorer=ref.restorer)
+    assert _streamed(case, 1, 3, overlap=overlap) == 0
+    _same(case, ref)
+    Hn.compare(case)
 
 
 def test_streamed_layer_subrange_and_pageable_host(cuda_device):
@@ -65,7 +83,7 @@ def test_streamed_full_size_7b(cuda_device):
     ref = Hn.run(Hn.make_case(w, cuda_device, gen_device=cuda_device))
     case = Hn.make_case(w, cuda_device, params=ref.params, restorer=ref.restorer,
                         gen_device=cuda_device)
-    assert _streamed(case, 4, 3) == 0
+    assert _streamed(case, 4, 3, overlap=True) == 0
     _same(case, ref)
 
 

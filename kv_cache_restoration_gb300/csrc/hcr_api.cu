@@ -402,7 +402,13 @@ hcr_status do_project_swap(hcr_handle* h, const RestoreArgs& a) {
   p.row_elems = d_kv;
   p.err = H.err;
   p.debug_stall = H.debug_stall;
-  const int grid = 2 * int(std::min<int64_t>(p.num_tiles, H.swap_clusters));
+  const int64_t units = std::min<int64_t>(p.num_tiles, H.swap_clusters);
+  // Tiles past the last whole round run as two half-chunk units each when
+  // that round then fits in half a tile's time on the pairs.
+  const int64_t rest = p.num_tiles % units;
+  p.split_tail =
+      (rest > 0 && 2 * rest <= units && p.chunk >= 32 && p.last_n >= 32) ? int32_t(rest) : 0;
+  const int grid = 2 * int(units);
   cudaError_t e = launch_project_swap(tmap_h, H.tmap_w5, p, grid, a.stream);
   if (e != cudaSuccess) return cuda_fail(e, "project launch (weight rows)");
   return HCR_OK;

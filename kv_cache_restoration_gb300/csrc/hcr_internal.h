@@ -184,6 +184,7 @@ struct ProjectParams {
   // hold `chunk` tokens (a multiple of 16, at most kSwapMaxChunk) except the
   // last, which holds last_n (a multiple of 16, at most chunk).
   int32_t chunk, n_chunks, last_n, head_pairs;
+  int32_t split_tail;   // the launch's last split_tail tiles run as two half-chunk units
   int32_t stages;   // ring depth (swap_stages(chunk))
   int32_t slot_cols, n_slots;   // TMEM accumulator ring: 2 x 256 or 3 x 160 columns
 };

@@ -88,6 +88,33 @@ __device__ __forceinline__ int chunk_tokens(const ProjectParams& p, int c) {
   return c == p.n_chunks - 1 ? p.last_n : p.chunk;
 }
 
+// A unit of work of a CTA pair: a tile, or half of one.  The last
+// p.split_tail tiles of the launch run as two units each, halves of their
+// token chunk (N rounded to multiples of 16), so that the pairs' last round
+// takes half a tile where it would leave most pairs idle for a whole one.
+// Units number num_tiles + split_tail.
+struct SwapUnit {
+  int l, hp;
+  int start, n;   // first token and token count
+};
+
+__device__ __forceinline__ SwapUnit swap_unit(int64_t u, const ProjectParams& p) {
+  const int64_t whole = p.num_tiles - p.split_tail;
+  const int64_t tile = u < whole ? u : whole + (u - whole) / 2;
+  const SwapCoord c = swap_coord(tile, p);
+  SwapUnit s{c.l, c.hp, c.c * p.chunk, chunk_tokens(p, c.c)};
+  if (u >= whole) {
+    const int n1 = (s.n / 2 + 15) & ~15;
+    if ((u - whole) & 1) {
+      s.start += n1;
+      s.n -= n1;
+    } else {
+      s.n = n1;
+    }
+  }
+  return s;
+}
+
 // N of the first MMA of a chunk of n tokens (the second has n - n1; none when
 // n1 == n): half the chunk, rounded up to a multiple of 16, when the chunk is
 // wider than one accumulator slot.
@@ -196,12 +223,13 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int64_t tile = unit; ok && tile < p.num_tiles; tile += units) {
-        const SwapCoord c = swap_coord(tile, p);
-        const int n = chunk_tokens(p, c.c);
-        // each CTA stages n/2 of the chunk's tokens (its box holds chunk/2 rows;
+      const int64_t n_units = p.num_tiles + p.split_tail;
+      for (int64_t tile = unit; ok && tile < n_units; tile += units) {
+        const SwapUnit c = swap_unit(tile, p);
+        const int n = c.n;
+        // each CTA stages n/2 of the unit's tokens (its box holds chunk/2 rows;
         // the MMAs read the first n/2)
-        const int row_b = c.c * p.chunk + int(rank) * (n >> 1);
+        const int row_b = c.start + int(rank) * (n >> 1);
         const int head = (p.layer_begin + c.l) * 2 * p.head_pairs + 2 * c.hp + int(rank);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase(ptx::smem_u32(&ps.empty[stage]), phase ^ 1u, abort, p,
@@ -240,8 +268,9 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
       int slot = 0;            // next slot of the ring
       uint32_t uses = 0;       // bit s: parity of slot s's uses so far
       bool ok = true;
-      for (int64_t tile = unit; ok && tile < p.num_tiles; tile += units) {
-        const int n = chunk_tokens(p, swap_coord(tile, p).c);
+      const int64_t n_units = p.num_tiles + p.split_tail;
+      for (int64_t tile = unit; ok && tile < n_units; tile += units) {
+        const int n = swap_unit(tile, p).n;
         const int n1 = first_mma_n(n, p.slot_cols), n2 = n - n1;
         const bool two = n2 > 0;
         const int s1 = slot, s2 = two ? (slot + 1) % p.n_slots : slot;
@@ -311,12 +340,13 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
     uint32_t uses = 0;
     uint32_t tab_phase = 0;
     bool ok_all = true;
-    for (int64_t tile = unit; ok_all && tile < p.num_tiles; tile += units) {
-      const SwapCoord c = swap_coord(tile, p);
-      const int n = chunk_tokens(p, c.c);
+    const int64_t n_units = p.num_tiles + p.split_tail;
+    for (int64_t tile = unit; ok_all && tile < n_units; tile += units) {
+      const SwapUnit c = swap_unit(tile, p);
+      const int n = c.n;
       const int n1 = first_mma_n(n, p.slot_cols);
       const bool two = n > n1;
-      const int start = c.c * p.chunk;
+      const int start = c.start;
       const int64_t srow = int64_t(c.l) * p.n_tokens;
       // The tile's per-token table, written while the MMA still works on the
       // tile: one coalesced round of loads instead of dependent loads per block.

@@ -318,3 +318,24 @@ def test_variant_policy_decisions(cuda_device):
     assert B.hcr_project_variant(r13.handle, 300, 40) == 3
     assert B.hcr_debug_set_variant(h, 3) == 0
     assert B.hcr_project_variant(h, 4096, 32) == 3
+
+
+# More weight-row tiles than CTA pairs: 2 layers x 40 head pairs = 80 tiles of
+# 300 tokens on 76 pairs, so the last 4 tiles run as two half-chunk units each
+# (160 + 144 tokens).  With two layers of 512 inputs the oracle checks every
+# element.
+SPLIT_TAIL = Workload("split-tail", ModelShape("st", 2, 512, 40, 40, 128), (300,), (11,))
+
+
+def test_weight_rows_with_split_tail_units(cuda_device):
+    from kv_cache_restoration_gb300 import binding as B
+    a = Hn.make_case(SPLIT_TAIL, cuda_device)
+    assert B.hcr_project_variant(a.restorer.handle, 300, 2) == 3
+    Hn.run(a)
+    assert a.status == 0, (a.status, a.flags)
+    Hn.compare(a)
+    b = Hn.make_case(SPLIT_TAIL, cuda_device, params=a.params, restorer=a.restorer)
+    assert B.hcr_debug_set_variant(b.restorer.handle, 2) == 0
+    Hn.run(b)
+    for c in ("k_cache", "v_cache"):
+        assert torch.equal(getattr(a, c).view(torch.int16), getattr(b, c).view(torch.int16)), c

@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
       __syncwarp();
       if (lane == 0) {
         if constexpr (PAIR)   // the leader's MMA reuses the accumulator in both CTAs
-          ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&ps.tempty[acc]), 0));
+          ptx::mbar_arrive_remote(ptx::mapa_shared(ptx::smem_u32(&ps.tempty[acc]), 0));
         else
           ptx::mbar_arrive(ptx::smem_u32(&ps.tempty[acc]));
       }

@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kEncThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0)
-        ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&es.tempty[acc]), 0));
+        ptx::mbar_arrive_remote(ptx::mapa_shared(ptx::smem_u32(&es.tempty[acc]), 0));
       if (++acc == kAccums) {
         acc = 0;
         acc_phase ^= 1u;

@@ -399,20 +399,9 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
         const int sl = slot;
         slot = (slot + 1) % p.n_slots;
         const int c_lo = part == 0 ? 0 : n1, c_hi = part == 0 ? n1 : n;
-        if (lane == 0)
-          ok = wait_phase(ptx::smem_u32(&ps.slot_full[sl]), (uses >> sl) & 1u, abort, p,
-                          kWaitEpilogueAccum, uint32_t(tile), uint32_t(sl));
-        uses ^= 1u << sl;
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          ok_all = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        const uint32_t tslot =
-            tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(sl * p.slot_cols);
         // RoPE (cos, sin) of this thread's two tokens and two frequencies in
-        // block bb, loaded two blocks ahead of their use (the loads miss L1)
+        // block bb, loaded two blocks ahead of their use (the loads miss L1;
+        // the first two blocks' before the slot is waited for)
         auto rope_load = [&](int bb, float2 (&cs)[2][2]) {
           const int ib = block_token(8 * bb, n, n1, start) - start + r2;
           const int pa = tab_pos[ib], pb = tab_pos[ib + 1];
@@ -431,6 +420,18 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
           if (b0 < b_end) rope_load(b0, cs_cur[0]);
           if (b0 + step < b_end) rope_load(b0 + step, cs_cur[1]);
         }
+        if (lane == 0)
+          ok = wait_phase(ptx::smem_u32(&ps.slot_full[sl]), (uses >> sl) & 1u, abort, p,
+                          kWaitEpilogueAccum, uint32_t(tile), uint32_t(sl));
+        uses ^= 1u << sl;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          ok_all = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t tslot =
+            tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(sl * p.slot_cols);
         for (int b = b0; b < b_end; b += 2 * step) {
           const int nw = b + step < b_end ? 2 : 1;   // blocks this iteration (warp-uniform)
           if (do_rope) {
@@ -508,7 +509,7 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0)   // the leader's MMA reuses the slot in both CTAs
-          ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&ps.slot_empty[sl]), 0));
+          ptx::mbar_arrive_remote(ptx::mapa_shared(ptx::smem_u32(&ps.slot_empty[sl]), 0));
       }
       if (!ok_all) break;
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ps.tab_free));

@@ -210,18 +210,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-// Arrive on an mbarrier that may live in another CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
 // Arrive on an mbarrier of another CTA of the cluster with the default
 // semantics (release at CTA scope): the writer's shared-memory stores are
-// performed in its own CTA before the arrival is sent.  Used where the
-// waiter's tensor-core operations read the writer's shared memory; the
-// cluster-scope release above costs about a microsecond per arrival, which a
-// per-stage signal cannot afford.
+// performed in its own CTA before the arrival is sent.  Two uses:
+// - a converter's A stage, which the waiter's tensor-core operations read;
+// - an epilogue's TMEM slot, whose tcgen05.ld reads have completed
+//   (tcgen05.wait::ld) before the arrival, which the waiter's MMA overwrites.
+// A cluster-scope release would also wait for the writer's earlier global
+// stores (the cache rows) and costs 0.6-1 us per arrival on the critical path.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }

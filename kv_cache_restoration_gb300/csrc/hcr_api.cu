@@ -310,9 +310,11 @@ bool use_pairs(const Handle& H, int32_t n_tokens, int32_t n_layers) {
 
 // Token chunks of the weight-row tiles: n_chunks chunks of `chunk` tokens (a
 // multiple of 16) and a last chunk of last_n (a multiple of 16), balanced so
-// padding stays below 16 tokens per chunk, on a TMEM ring of n_slots slots of
-// slot_cols columns: 257..320 tokens as one chunk on three 160-column slots,
-// everything else as chunks of at most 256 on two 256-column slots.
+// padding stays below 16 tokens per chunk, on TMEM accumulator slots of
+// slot_cols columns: everything up to 256 tokens per chunk on two 256-column
+// slots, and 257..320 tokens as one chunk on two big slots of the largest
+// multiple of 32 columns that leaves room for the chunk's remaining columns in
+// a third, small slot after them (192 + 192 + 112 columns for 304 tokens).
 struct SwapPlan {
   int32_t chunk = 0, n_chunks = 0, last_n = 0, slot_cols = 0, n_slots = 0;
   bool ok = false;
@@ -323,7 +325,6 @@ SwapPlan swap_plan(int32_t n_tokens) {
   if (n_tokens <= 0) return s;
   const int64_t T = n_tokens;
   const bool ring3 = T > kBlockN && T <= kSwapMaxChunk;
-  s.slot_cols = ring3 ? 160 : kBlockN;
   s.n_slots = ring3 ? 3 : 2;
   const int64_t max_chunk = ring3 ? kSwapMaxChunk : kBlockN;
   s.n_chunks = int32_t((T + max_chunk - 1) / max_chunk);
@@ -331,7 +332,10 @@ SwapPlan swap_plan(int32_t n_tokens) {
   s.chunk = int32_t((per + 15) / 16 * 16);
   const int64_t rest = T - int64_t(s.n_chunks - 1) * s.chunk;
   s.last_n = int32_t((rest + 15) / 16 * 16);
-  s.ok = s.chunk >= 16 && s.chunk <= max_chunk && rest > 0 && s.last_n <= s.chunk;
+  s.slot_cols = ring3 ? (kSwapTmemCols - s.chunk) / 32 * 32 : kBlockN;
+  s.ok = s.chunk >= 16 && s.chunk <= max_chunk && rest > 0 && s.last_n <= s.chunk &&
+         (!ring3 || (s.chunk - s.slot_cols >= 16 && 2 * s.slot_cols + (s.chunk - s.slot_cols) <=
+                                                        kSwapTmemCols));
   return s;
 }
 

@@ -43,9 +43,10 @@ static_assert(kSmemSingle <= 232448 - 512 && kSmemPair <= 232448 - 512,
 // regime the ring depth sets how many weight bytes are in flight from HBM.
 constexpr int kSwapEpilogueWarps = 8;
 constexpr int kSwapThreads = 64 + 32 * kSwapEpilogueWarps;
-// TMEM holds a ring of accumulator slots, one MMA's N each: two slots of 256
-// columns (a tile of up to 256 tokens takes one), or three of 160 (a tile of
-// up to 320 tokens takes two).
+// TMEM holds accumulator slots, one MMA's N each: two slots of 256 columns (a
+// tile of up to 256 tokens takes one), or for tiles of 257..320 tokens two big
+// slots taken in turn plus a small slot after them (a tile takes its big slot
+// and the small one).
 constexpr int kSwapSlotsMax = 3;
 constexpr int kSwapTmemCols = 512;     // allocated (a power of two >= the ring)
 constexpr int kSwapMaxChunk = 320;     // tokens per tile (three-slot ring)
@@ -186,7 +187,7 @@ struct ProjectParams {
   int32_t chunk, n_chunks, last_n, head_pairs;
   int32_t split_tail;   // the launch's last split_tail tiles run as two half-chunk units
   int32_t stages;   // ring depth (swap_stages(chunk))
-  int32_t slot_cols, n_slots;   // TMEM accumulator ring: 2 x 256 or 3 x 160 columns
+  int32_t slot_cols, n_slots;   // TMEM slots: 2 x 256, or 2 big of slot_cols + 1 small
 };
 
 // Launchers (return cudaGetLastError() of the launch).

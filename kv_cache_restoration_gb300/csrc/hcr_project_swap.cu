@@ -44,12 +44,17 @@
 // same order by the epilogue:
 //   * two slots of 256 columns, one per tile of up to 256 tokens: the
 //     epilogue of a tile overlaps the whole mainloop of the next;
-//   * three slots of 160 columns, two per tile of up to 320 tokens (two MMAs,
-//     N = n1 + n2): the next tile's first slot is free while the epilogue
-//     drains the previous tile, and its second is the previous tile's first,
-//     which the epilogue drains first -- the MMA waits for about half of one
-//     tile's epilogue.  It is the ring for restores of 257..320 tokens, which
-//     otherwise run as two ingress-bound chunks of 160 or less.
+//   * for tiles of 257..320 tokens, two "big" slots of b columns (b the
+//     largest multiple of 32 with b + n <= 512: 192 for 304 tokens) taken in
+//     turn, and one "small" slot after them: a tile puts its first n - b
+//     columns (the first MMA) in the small slot and the other b (the second
+//     MMA) in its big slot, and the epilogue drains the small part first.
+//     The next tile's big slot is free while the epilogue drains the
+//     previous tile, and its small slot is the part the epilogue drains
+//     first -- the MMA waits for the drain of n - b columns (112 of 304),
+//     about a third of one tile's epilogue.  It is the ring for restores of
+//     257..320 tokens, which otherwise run as two ingress-bound chunks of
+//     160 or less.
 //
 // With two MMAs, CTA r of the pair stages the chunk's tokens
 // [r n/2, (r+1) n/2) as rows 0 .. n/2-1; the first MMA reads rows [0, n1/2) of
@@ -115,11 +120,17 @@ __device__ __forceinline__ SwapUnit swap_unit(int64_t u, const ProjectParams& p)
   return s;
 }
 
-// N of the first MMA of a chunk of n tokens (the second has n - n1; none when
-// n1 == n): half the chunk, rounded up to a multiple of 16, when the chunk is
-// wider than one accumulator slot.
+// N of the first MMA of a unit of n tokens on slots of slot_cols columns
+// (the second has n - n1; none when n1 == n): a unit wider than one slot puts
+// its first n - slot_cols columns in the small slot.
 __device__ __forceinline__ int first_mma_n(int n, int slot_cols) {
-  return n <= slot_cols ? n : ((n / 2 + 15) & ~15);
+  return n <= slot_cols ? n : n - slot_cols;
+}
+
+// TMEM column of accumulator slot s: big slots 0 and 1 at s * slot_cols, the
+// small slot (2) after them.
+__device__ __forceinline__ uint32_t slot_col(int s, const ProjectParams& p) {
+  return uint32_t(s * p.slot_cols);
 }
 
 // The MMAs of one k-block: four K = 16 steps, each one MMA (TWO = false) or
@@ -265,7 +276,7 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
       constexpr uint32_t idesc_m256 = make_idesc_f16(DT, 2 * kBlockM, 0);   // N filled per tile
       int stage = 0;
       uint32_t phase = 0;
-      int slot = 0;            // next slot of the ring
+      int big = 0;             // this unit's big slot (0, 1 in turn)
       uint32_t uses = 0;       // bit s: parity of slot s's uses so far
       bool ok = true;
       const int64_t n_units = p.num_tiles + p.split_tail;
@@ -273,7 +284,7 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
         const int n = swap_unit(tile, p).n;
         const int n1 = first_mma_n(n, p.slot_cols), n2 = n - n1;
         const bool two = n2 > 0;
-        const int s1 = slot, s2 = two ? (slot + 1) % p.n_slots : slot;
+        const int s1 = two ? 2 : big, s2 = big;   // first MMA: the small slot if two
         // the slots must be drained of their previous tiles (free on first use)
         if (!wait_phase(ptx::smem_u32(&ps.slot_empty[s1]), ((uses >> s1) & 1u) ^ 1u, abort, p,
                         kWaitMmaAccum, uint32_t(tile), uint32_t(s1)))
@@ -282,8 +293,8 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
                                abort, p, kWaitMmaAccum, uint32_t(tile), uint32_t(s2)))
           break;
         ptx::tc_fence_after();
-        const uint32_t d1 = tmem_base + uint32_t(s1 * p.slot_cols);
-        const uint32_t d2 = tmem_base + uint32_t(s2 * p.slot_cols);
+        const uint32_t d1 = tmem_base + slot_col(s1, p);
+        const uint32_t d2 = tmem_base + slot_col(s2, p);
         const uint32_t id1 = idesc_m256 | (uint32_t(n1 >> 3) << 17);
         const uint32_t id2 = idesc_m256 | (uint32_t(n2 >> 3) << 17);
         const uint32_t b_off2 = uint32_t(n1 / 2) * kBlockK * 2;   // second MMA's token rows
@@ -313,7 +324,7 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
           ptx::mma_commit_pair_multicast(ptx::smem_u32(&ps.slot_full[s2]), 0x3);
           uses ^= 1u << s2;
         }
-        slot = (s2 + 1) % p.n_slots;
+        big ^= 1;
       }
       // Every MMA this thread issued has completed once `drain` flips.
       ptx::mma_commit_pair_multicast(ptx::smem_u32(&ps.drain), 0x1);
@@ -336,7 +347,7 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
     const int piece = lane & 3;              // matrix: (lane group piece>>1, dims hi if piece&1)
     const int dim0 = 64 * (piece & 1) + 8 * (2 * quad + (piece >> 1));
     const bool ln = p.layer_norm != 0;
-    int slot = 0;            // the MMA issuer's ring, followed in the same order
+    int big = 0;             // the unit's big slot, in the MMA issuer's order
     uint32_t uses = 0;
     uint32_t tab_phase = 0;
     bool ok_all = true;
@@ -394,10 +405,10 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
       uint16_t* base = reinterpret_cast<uint16_t*>(is_k ? p.k_cache : p.v_cache) +
                        int64_t(c.l) * p.layer_stride + int64_t(kvh) * kHead + dim0;
 
-      // the tile's one or two slots, drained in the order the next tiles need them
+      // the unit's one or two slots, drained in the order the next units need
+      // them: the small slot (the first MMA's columns) before the big one
       for (int part = 0; part < (two ? 2 : 1); ++part) {
-        const int sl = slot;
-        slot = (slot + 1) % p.n_slots;
+        const int sl = (two && part == 0) ? 2 : big;
         const int c_lo = part == 0 ? 0 : n1, c_hi = part == 0 ? n1 : n;
         // RoPE (cos, sin) of this thread's two tokens and two frequencies in
         // block bb, loaded two blocks ahead of their use (the loads miss L1;
@@ -431,7 +442,7 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
         }
         ptx::tc_fence_after();
         const uint32_t tslot =
-            tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(sl * p.slot_cols);
+            tmem_base + (uint32_t(quad * 32) << 16) + slot_col(sl, p);
         for (int b = b0; b < b_end; b += 2 * step) {
           const int nw = b + step < b_end ? 2 : 1;   // blocks this iteration (warp-uniform)
           if (do_rope) {
@@ -512,6 +523,7 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
           ptx::mbar_arrive_remote(ptx::mapa_shared(ptx::smem_u32(&ps.slot_empty[sl]), 0));
       }
       if (!ok_all) break;
+      big ^= 1;
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ps.tab_free));
       tab_phase ^= 1u;
     }

@@ -339,3 +339,30 @@ def test_weight_rows_with_split_tail_units(cuda_device):
     Hn.run(b)
     for c in ("k_cache", "v_cache"):
         assert torch.equal(getattr(a, c).view(torch.int16), getattr(b, c).view(torch.int16)), c
+
+
+# The three-slot TMEM layout for chunks of 257..320 tokens: two big slots taken
+# in turn and a small slot for each tile's first columns.  Each token count
+# gives a different split of its chunk (big + small columns): 257 -> 272 =
+# 224 + 48, 288 = 224 + 64, 300 -> 304 = 192 + 112, 320 = 192 + 128.  Four
+# layers of 40 head pairs are 160 tiles on 76 pairs, so every pair runs two or
+# three units in turn (both big slots, the small slot reused) and the last 8
+# tiles split in halves.
+RING3_TOKENS = [257, 288, 300, 320]
+
+
+@pytest.mark.parametrize("n_tokens", RING3_TOKENS)
+def test_weight_rows_three_slot_layout(cuda_device, n_tokens):
+    from kv_cache_restoration_gb300 import binding as B
+    w = Workload(f"ring3-{n_tokens}", ModelShape("r3", 4, 512, 40, 40, 128), (n_tokens,), (5,),
+                 block_order="shuffled")
+    a = Hn.make_case(w, cuda_device)
+    assert B.hcr_project_variant(a.restorer.handle, n_tokens, 4) == 3
+    Hn.run(a)
+    assert a.status == 0, (a.status, a.flags)
+    Hn.compare(a)
+    b = Hn.make_case(w, cuda_device, params=a.params, restorer=a.restorer)
+    assert B.hcr_debug_set_variant(b.restorer.handle, 2) == 0
+    Hn.run(b)
+    for c in ("k_cache", "v_cache"):
+        assert torch.equal(getattr(a, c).view(torch.int16), getattr(b, c).view(torch.int16)), c

@@ -595,6 +595,20 @@ hcr_status hcr_debug_set_stall(hcr_handle* h, int32_t enable);
 hcr_status hcr_debug_set_variant(hcr_handle* h, int32_t variant);
 
 /*
+ * hcr_debug_swap_plan -- testing hook (host-only, no handle, no CUDA call):
+ * the token chunks and TMEM accumulator slots the weight-row tiles (variant
+ * 3) would use for a projection of n_tokens tokens.  Writes out[6] = {chunk,
+ * n_chunks, last_n, slot_cols, n_slots, ok}: n_chunks - 1 chunks of `chunk`
+ * tokens and a last one of last_n (both multiples of 16); n_slots == 2: two
+ * slots of slot_cols (256) TMEM columns, one per tile; n_slots == 3 (one
+ * chunk of 257..320 tokens): two big slots of slot_cols columns taken in turn
+ * and a small slot at column 2 * slot_cols for each tile's first
+ * chunk - slot_cols columns.  ok is 0 when the variant cannot take the count.
+ * HCR_ERR_INVALID_ARG if out is NULL.
+ */
+hcr_status hcr_debug_swap_plan(int32_t n_tokens, int32_t* out);
+
+/*
  * hcr_debug_timeout_record -- diagnostics for HCR_ERR_TIMEOUT: synchronise
  * `stream`, copy the record of the first pipeline wait that gave up since the
  * last call into out[6] = {which wait (0: none), CTA, thread, a, b, parity}

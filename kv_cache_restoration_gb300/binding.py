@@ -157,6 +157,8 @@ lib.hcr_num_sms.argtypes = [_vp]
 lib.hcr_num_sms.restype = _i32
 lib.hcr_debug_timeout_record.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]
 lib.hcr_debug_timeout_record.restype = ctypes.c_int
+lib.hcr_debug_swap_plan.argtypes = [_i32, _vp]
+lib.hcr_debug_swap_plan.restype = ctypes.c_int
 lib.hcr_debug_set_variant.argtypes = [_vp, _i32]
 lib.hcr_debug_set_variant.restype = ctypes.c_int
 lib.hcr_debug_set_stall.argtypes = [_vp, _i32]
@@ -455,6 +457,16 @@ def hcr_project_variant(handle, n_tokens: int, n_layers: int) -> int:
     """Tile variant the projection uses: 1 single CTAs, 2 CTA pairs, 3 CTA pairs
     with weight rows as M and chunks of up to 320 tokens as N (host-only)."""
     return lib.hcr_project_variant(handle, n_tokens, n_layers)
+
+
+def hcr_debug_swap_plan(n_tokens: int) -> dict:
+    """The weight-row tiles' chunks and TMEM slots for n_tokens (host-only)."""
+    out = (ctypes.c_int32 * 6)()
+    st = lib.hcr_debug_swap_plan(n_tokens, out)
+    if st != 0:
+        raise RuntimeError(hcr_last_error())
+    keys = ("chunk", "n_chunks", "last_n", "slot_cols", "n_slots", "ok")
+    return dict(zip(keys, (int(v) for v in out)))
 
 
 def hcr_num_sms(handle) -> int:

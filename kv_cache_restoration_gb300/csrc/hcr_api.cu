@@ -937,6 +937,18 @@ hcr_status hcr_save_kv(hcr_handle* h, void* kv, int32_t layer_begin, int32_t lay
   return kv_rows(h, a, /*to_cache=*/false, "kv");
 }
 
+hcr_status hcr_debug_swap_plan(int32_t n_tokens, int32_t* out) {
+  if (!out) return fail(HCR_ERR_INVALID_ARG, "out is NULL");
+  const SwapPlan sp = swap_plan(n_tokens);
+  out[0] = sp.chunk;
+  out[1] = sp.n_chunks;
+  out[2] = sp.last_n;
+  out[3] = sp.slot_cols;
+  out[4] = sp.n_slots;
+  out[5] = sp.ok ? 1 : 0;
+  return HCR_OK;
+}
+
 int32_t hcr_project_variant(const hcr_handle* h, int32_t n_tokens, int32_t n_layers) {
   if (!h || n_tokens <= 0 || n_layers <= 0) return 0;
   return choose_variant(h->impl, n_tokens, n_layers);

@@ -273,9 +273,11 @@ struct VariantPolicy {
   // the pairs' 256-row tiles (counting the pairs' half tail tile as 128 rows).
   double pair_pad_ratio = 0.9;
   // Weight rows as M for 257..320 tokens (one chunk of up to 320 on the
-  // three-slot TMEM ring): 7B 0.526 against 0.576 ms (pairs), 13B 0.974
+  // three-slot TMEM layout): 7B 0.526 against 0.576 ms (pairs), 13B 0.974
   // against 1.080 (single CTAs), OPT-30B 2.33 against 2.54 ms (single CTAs);
-  // from 384 tokens the token-row pairs were 5-10% faster.
+  // from 384 tokens the token-row pairs were faster (7B, one session: 384
+  // tokens 0.632 against 0.659 ms, 512 0.703/0.742, 794 1.272/1.299, 1024
+  // 1.366/1.445, 1536 2.034/2.137).
   int32_t rows_min_tokens = kBlockN + 1;
   int32_t rows_max_tokens = kSwapMaxChunk;
 };

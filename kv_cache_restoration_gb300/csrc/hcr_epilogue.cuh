@@ -37,6 +37,18 @@ __device__ __forceinline__ TileCoord tile_coord(int64_t tile, const ProjectParam
   return c;
 }
 
+// Tile of round k for scheduling unit `unit` of `units` (a CTA or a CTA
+// pair of the persistent grid): round k covers the tiles [k units,
+// (k + 1) units), the set a plain stride would give it, with the unit's place
+// in it rotated by k.  With a plain stride a unit keeps its place in every
+// round, so when units is a multiple of the layer's m-tiles (76 pairs and 4
+// m-tiles at 794 tokens) every tile a unit gets has the same m: the units
+// that get the cheap half tail tiles idle while the others run only full
+// tiles.  Rotating gives each unit every place in turn.
+__device__ __forceinline__ int64_t round_tile(int64_t k, int64_t unit, int64_t units) {
+  return k * units + (unit + k) % units;
+}
+
 // Epilogue of one finished tile, run by each of the four epilogue warps of a
 // CTA on its 32-lane TMEM quadrant `quad` (tacc: the accumulator's TMEM
 // address with the quadrant's lane offset).

@@ -366,3 +366,25 @@ def test_weight_rows_three_slot_layout(cuda_device, n_tokens):
     Hn.run(b)
     for c in ("k_cache", "v_cache"):
         assert torch.equal(getattr(a, c).view(torch.int16), getattr(b, c).view(torch.int16)), c
+
+
+# CTA pairs over several rounds of the persistent grid, with a half tail tile
+# per layer: 4 layers x 32 n-tiles x 4 m-tiles (794 tokens) = 512 tiles, and x
+# 2 m-tiles (384 tokens) = 256 tiles, on 76 pairs, so every pair runs several
+# tiles and the last round is partial.  Each pair's place in a round rotates,
+# so its tiles mix full and half tail m-tiles.
+@pytest.mark.parametrize("n_tokens", [794, 384])
+def test_pair_rounds_with_half_tails(cuda_device, n_tokens):
+    from kv_cache_restoration_gb300 import binding as B
+    w = Workload(f"rounds-{n_tokens}", ModelShape("rd", 4, 512, 32, 32, 128), (n_tokens,), (3,),
+                 block_order="shuffled")
+    a = Hn.make_case(w, cuda_device)
+    assert B.hcr_debug_set_variant(a.restorer.handle, 2) == 0
+    Hn.run(a)
+    assert a.status == 0, (a.status, a.flags)
+    Hn.compare(a)
+    b = Hn.make_case(w, cuda_device, params=a.params, restorer=a.restorer)
+    assert B.hcr_debug_set_variant(b.restorer.handle, 1) == 0
+    Hn.run(b)
+    for c in ("k_cache", "v_cache"):
+        assert torch.equal(getattr(a, c).view(torch.int16), getattr(b, c).view(torch.int16)), c

@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int64_t k = 0, tile; ok && (tile = round_tile(k, unit, units)) < p.num_tiles; ++k) {
+      for (int64_t rnd = 0, tile; ok && (tile = round_tile(rnd, unit, units)) < p.num_tiles; ++rnd) {
         const TileCoord c = tile_coord(tile, p);
         // a half tail tile stages 64 rows of A per CTA (M=128 across the pair)
         const bool half_tile = HT && c.m == p.m_tiles - 1;
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int64_t k = 0, tile; ok && (tile = round_tile(k, unit, units)) < p.num_tiles; ++k) {
+      for (int64_t rnd = 0, tile; ok && (tile = round_tile(rnd, unit, units)) < p.num_tiles; ++rnd) {
         if (!wait_phase(ptx::smem_u32(&ps.tempty[acc]), acc_phase ^ 1u, abort, p, kWaitMmaAccum,
                         uint32_t(tile), uint32_t(acc)))
           break;
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
     const int quad = warp & 3;               // TMEM lanes [32*quad, 32*quad+32)
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t k = 0, tile; (tile = round_tile(k, unit, units)) < p.num_tiles; ++k) {
+    for (int64_t rnd = 0, tile; (tile = round_tile(rnd, unit, units)) < p.num_tiles; ++rnd) {
       const TileCoord c = tile_coord(tile, p);
       int ok = 0;
       if (lane == 0)

@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kEncThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int64_t tile = unit; ok && tile < p.num_tiles; tile += units) {
+      for (int64_t rnd = 0, tile; ok && (tile = round_tile(rnd, unit, units)) < p.num_tiles; ++rnd) {
         const TileCoord c = tile_coord(tile, p);
         const int row_b = c.n * kBlockN + int(rank) * (kBlockN / 2);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kEncThreads, 1)
       int cs = 0;
       uint32_t cphase = 0;
       bool ok = true;
-      for (int64_t tile = unit; ok && tile < p.num_tiles; tile += units) {
+      for (int64_t rnd = 0, tile; ok && (tile = round_tile(rnd, unit, units)) < p.num_tiles; ++rnd) {
         const TileCoord c = tile_coord(tile, p);
         const bool half_tile = HT && c.m == p.m_tiles - 1;
         const int row_a = c.m * 2 * kBlockM + int(rank) * (half_tile ? kBlockM / 2 : kBlockM);
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kEncThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int64_t tile = unit; ok && tile < p.num_tiles; tile += units) {
+      for (int64_t rnd = 0, tile; ok && (tile = round_tile(rnd, unit, units)) < p.num_tiles; ++rnd) {
         if (!wait_phase_sleep(ptx::smem_u32(&es.tempty[acc]), acc_phase ^ 1u, abort, p,
                               kWaitMmaAccum, uint32_t(tile), uint32_t(acc), kSleepNs))
           break;
@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(kEncThreads, 1)
     const int quad = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t tile = unit; tile < p.num_tiles; tile += units) {
+    for (int64_t rnd = 0, tile; (tile = round_tile(rnd, unit, units)) < p.num_tiles; ++rnd) {
       const TileCoord c = tile_coord(tile, p);
       int ok = 0;
       if (lane == 0)
@@ -417,11 +417,12 @@ __global__ void __launch_bounds__(kEncThreads, 1)
     const int r0 = kGroupRows * (cw % kGroupWarps) + kRunRows * (lane >> 2);
     int kb = grp, stage = grp, cs = grp;
     uint32_t phase = 0, cphase = 0;
-    int64_t tile = unit;
+    int64_t rnd = 0;               // the unit's tiles in the other roles' order
     while (kb >= p.k_blocks) {   // fewer k-blocks per tile than groups
       kb -= p.k_blocks;
-      tile += units;
+      ++rnd;
     }
+    int64_t tile = round_tile(rnd, unit, units);
     int64_t run_tile = -1;
     Run run;
     TileCoord c{};
@@ -466,8 +467,9 @@ __global__ void __launch_bounds__(kEncThreads, 1)
       kb += kConvGroups;
       while (kb >= p.k_blocks) {
         kb -= p.k_blocks;
-        tile += units;
+        ++rnd;
       }
+      tile = round_tile(rnd, unit, units);
       stage += kConvGroups;
       while (stage >= S) {
         stage -= S;

@@ -131,9 +131,14 @@ hcr_status hcr_create(const hcr_model_dims* dims, const void* const* gamma,
 void hcr_destroy(hcr_handle* h);
 
 /*
- * hcr_workspace_bytes -- device scratch a restore of n_tokens tokens over
- * n_layers_in_range layers needs (per-token slot and position, per-row norm
- * statistics).  Returns 0 for invalid arguments or an empty restore.
+ * hcr_workspace_bytes -- device scratch for a restore of n_tokens tokens over
+ * n_layers_in_range layers: per-token slot and position, per-row norm
+ * statistics, and one int32 flag per 16 tokens and layer.  With the flags'
+ * room the projection computes most layers' norm statistics itself
+ * (hcr_debug_fused_stats); a restore also accepts the smaller workspace
+ * without them (this size minus the flags, rounded to 256 bytes) and then
+ * computes every layer's statistics in its prepare kernel.  Returns 0 for
+ * invalid arguments or an empty restore.
  */
 size_t hcr_workspace_bytes(const hcr_handle* h, int32_t n_tokens, int32_t n_layers_in_range);
 
@@ -593,6 +598,25 @@ hcr_status hcr_debug_set_stall(hcr_handle* h, int32_t enable);
  * a restore through the handle may be enqueued.
  */
 hcr_status hcr_debug_set_variant(hcr_handle* h, int32_t variant);
+
+/*
+ * hcr_debug_fused_stats -- testing hook (host-only): whether a restore of
+ * n_tokens tokens over n_layers layers with a workspace of workspace_bytes
+ * computes most of its norm statistics inside the projection kernel.
+ * Returns 0 when it does not (the prepare kernel computes every layer's);
+ * otherwise L0 >= 1: the prepare kernel computes layers [0, L0) of the call
+ * and the projection's statistics warps the rest, each tile's epilogue
+ * waiting (bounded) for its rows.  The results are the same bits either way.
+ * It does when the projection runs token-row tiles (variants 1 and 2) of at
+ * most 8 m-tiles per layer (2048 tokens for CTA pairs, 1024 for single
+ * CTAs; above that the projection runs at its per-SM ingress limit and the
+ * statistics' reads would cost it what the prepare pass does), the call has
+ * more layers than the projection's first three rounds of tiles reach, and
+ * workspace_bytes >= hcr_workspace_bytes (which includes room for the
+ * per-16-token flags; the smaller minimum workspace disables it).
+ */
+int32_t hcr_debug_fused_stats(const hcr_handle* h, int32_t n_tokens, int32_t n_layers,
+                              size_t workspace_bytes);
 
 /*
  * hcr_debug_swap_plan -- testing hook (host-only, no handle, no CUDA call):

@@ -157,6 +157,8 @@ lib.hcr_num_sms.argtypes = [_vp]
 lib.hcr_num_sms.restype = _i32
 lib.hcr_debug_timeout_record.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]
 lib.hcr_debug_timeout_record.restype = ctypes.c_int
+lib.hcr_debug_fused_stats.argtypes = [_vp, _i32, _i32, ctypes.c_size_t]
+lib.hcr_debug_fused_stats.restype = _i32
 lib.hcr_debug_swap_plan.argtypes = [_i32, _vp]
 lib.hcr_debug_swap_plan.restype = ctypes.c_int
 lib.hcr_debug_set_variant.argtypes = [_vp, _i32]
@@ -457,6 +459,12 @@ def hcr_project_variant(handle, n_tokens: int, n_layers: int) -> int:
     """Tile variant the projection uses: 1 single CTAs, 2 CTA pairs, 3 CTA pairs
     with weight rows as M and chunks of up to 320 tokens as N (host-only)."""
     return lib.hcr_project_variant(handle, n_tokens, n_layers)
+
+
+def hcr_debug_fused_stats(handle, n_tokens: int, n_layers: int, workspace_bytes: int) -> int:
+    """0, or the layers the prepare kernel still computes when the projection
+    computes the rest of the norm statistics (host-only)."""
+    return lib.hcr_debug_fused_stats(handle, n_tokens, n_layers, workspace_bytes)
 
 
 def hcr_debug_swap_plan(n_tokens: int) -> dict:

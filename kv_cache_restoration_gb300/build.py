@@ -23,7 +23,7 @@ SOURCES = ["hcr_api.cu", "hcr_prepare.cu", "hcr_project.cu", "hcr_project_swap.c
            "hcr_project_enc.cu", "hcr_no_alloc.cu",
            "hcr_streamed.cu", "hcr_save.cu", "hcr_kv.cu", "hcr_plan.cu",
            "hcr_codec.cu"]
-HEADERS = ["hcr_internal.h", "hcr_host.h", "hcr_pipe.cuh", "hcr_epilogue.cuh",
+HEADERS = ["hcr_internal.h", "hcr_host.h", "hcr_pipe.cuh", "hcr_epilogue.cuh", "hcr_stats.cuh",
            "hcr_decode.cuh", "ptx.cuh"]
 
 NVCC_FLAGS = [

@@ -203,6 +203,19 @@ hcr_status validate_restore(const hcr_handle* h, const RestoreArgs& a, bool* emp
   return HCR_OK;
 }
 
+// Norm statistics fused into the token-row projection: the prepare kernel
+// computes the first layer0 layers of the call (those the projection's first
+// three rounds of tiles reach) and the projection's statistics warps the rest,
+// items of kStatsItemRows tokens per layer.  On when the projection runs
+// token-row tiles, the call covers more layers than that, its statistics live
+// in the workspace and the workspace has room for the flags.
+struct FusedStats {
+  bool on = false;
+  int32_t layer0 = 0, items = 0;
+};
+constexpr int64_t kFusedStatsMaxMTiles = 8;   // token m-tiles per layer
+FusedStats fused_stats(const Handle& H, const RestoreArgs& a);
+
 // stats = false: the slot map only (the K/V row copies need no statistics).
 // enc: the statistics of the rows decoded from the codec's form, and each
 // token's group anchor for the projection (a.hidden is then unused).
@@ -247,6 +260,14 @@ hcr_status do_prepare(hcr_handle* h, const RestoreArgs& a, bool stats = true,
   if (enc) {
     p.enc = *enc;
     p.enc.anchor = reinterpret_cast<int32_t*>(ws + w.anchor_off);
+  }
+  if (stats && !enc && !stats_rstd) {
+    const FusedStats fs = fused_stats(H, a);
+    if (fs.on) {
+      p.n_layers = fs.layer0;
+      p.zero_flags = reinterpret_cast<int32_t*>(ws + w.flags_off);
+      p.n_zero_flags = int64_t(nl) * fs.items;
+    }
   }
   cudaError_t e = launch_prepare(p, a.stream);
   if (e != cudaSuccess) return cuda_fail(e, "prepare launch");
@@ -354,6 +375,34 @@ int32_t choose_variant(const Handle& H, int32_t n_tokens, int32_t n_layers) {
   if (H.variant == 2) v = H.pair_clusters > 0 ? 2 : 1;
   if (H.variant == 3 && swap_ok) v = 3;
   return v;
+}
+
+FusedStats fused_stats(const Handle& H, const RestoreArgs& a) {
+  FusedStats f;
+  const hcr_model_dims& d = H.dims;
+  const int32_t nl = a.layer_end - a.layer_begin;
+  if (nl < 2 || a.rstd || a.n_tokens <= 0) return f;
+  const int32_t v = choose_variant(H, a.n_tokens, nl);
+  if (v != 1 && v != 2) return f;
+  if (a.workspace_bytes < workspace_layout(a.n_tokens, nl, d.norm == HCR_NORM_LAYER).total_fused)
+    return f;
+  const int64_t tile_m = v == 2 ? 2 * kBlockM : kBlockM;
+  const int64_t m_tiles = (a.n_tokens + tile_m - 1) / tile_m;
+  // With more m-tiles per layer the projection runs at its per-SM ingress
+  // limit and the statistics warps' reads cost it what the prepare pass would
+  // (7B, CTA pairs, alternating builds: 1100 tokens 1.548/1.561 against
+  // 1.589/1.601 ms per step, 2048 tokens 2.695/2.707 against 2.703/2.747,
+  // 4096 tokens 5.555/5.526 against 5.489/5.518).
+  if (m_tiles > kFusedStatsMaxMTiles) return f;
+  const int64_t n_tiles = (2 * int64_t(d.n_kv_heads) * d.head_dim + kBlockN - 1) / kBlockN;
+  const int64_t per_layer = m_tiles * n_tiles;
+  const int64_t units = std::min<int64_t>(per_layer * nl, v == 2 ? H.pair_clusters : H.num_sms);
+  const int64_t layer0 = std::max<int64_t>(1, (3 * units + per_layer - 1) / per_layer);
+  if (layer0 >= nl) return f;
+  f.on = true;
+  f.layer0 = int32_t(layer0);
+  f.items = (a.n_tokens + kStatsItemRows - 1) / kStatsItemRows;
+  return f;
 }
 
 hcr_status do_project_swap(hcr_handle* h, const RestoreArgs& a) {
@@ -481,7 +530,16 @@ hcr_status do_project(hcr_handle* h, const RestoreArgs& a) {
   if (st != HCR_OK) return st;
 
   const bool pair = variant == 2;
-  const ProjectParams p = token_row_params(H, a, pair, false);
+  ProjectParams p = token_row_params(H, a, pair, false);
+  const FusedStats fs = fused_stats(H, a);
+  if (fs.on) {
+    const WorkspaceLayout w = workspace_layout(a.n_tokens, nl, d.norm == HCR_NORM_LAYER);
+    p.stats_flags = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a.workspace) + w.flags_off);
+    p.stats_layer0 = fs.layer0;
+    p.stats_items = fs.items;
+    p.hidden_rows = a.hidden;
+    p.eps = d.norm_eps;
+  }
   const int grid = pair ? 2 * int(std::min<int64_t>(p.num_tiles, H.pair_clusters))
                         : int(std::min<int64_t>(p.num_tiles, H.num_sms));
   CUtensorMap tmap_h64 = tmap_h;
@@ -539,6 +597,11 @@ hcr_status do_project_enc(hcr_handle* h, const RestoreArgs& a, const CodecInput&
 }
 
 }  // namespace
+
+size_t workspace_min_bytes(const hcr_handle* h, int32_t n_tokens, int32_t n_layers) {
+  if (!h || n_tokens <= 0 || n_layers <= 0) return 0;
+  return workspace_layout(n_tokens, n_layers, h->impl.dims.norm == HCR_NORM_LAYER).total;
+}
 
 // Pieces of hcr_restore for the layer-pipelined restores (hcr_streamed.cu).
 hcr_status pipeline_placement(hcr_handle* h, const void* staging, int32_t layer_begin,
@@ -770,7 +833,8 @@ void hcr_destroy(hcr_handle* h) {
 
 size_t hcr_workspace_bytes(const hcr_handle* h, int32_t n_tokens, int32_t n_layers_in_range) {
   if (!h || n_tokens <= 0 || n_layers_in_range <= 0) return 0;
-  return workspace_layout(n_tokens, n_layers_in_range, h->impl.dims.norm == HCR_NORM_LAYER).total;
+  return workspace_layout(n_tokens, n_layers_in_range, h->impl.dims.norm == HCR_NORM_LAYER)
+      .total_fused;
 }
 
 #define HCR_RESTORE_ARGS                                                                         \
@@ -949,6 +1013,18 @@ hcr_status hcr_debug_swap_plan(int32_t n_tokens, int32_t* out) {
   out[4] = sp.n_slots;
   out[5] = sp.ok ? 1 : 0;
   return HCR_OK;
+}
+
+int32_t hcr_debug_fused_stats(const hcr_handle* h, int32_t n_tokens, int32_t n_layers,
+                              size_t workspace_bytes) {
+  if (!h || n_tokens <= 0 || n_layers <= 0) return 0;
+  RestoreArgs a{};
+  a.layer_begin = 0;
+  a.layer_end = n_layers;
+  a.n_tokens = n_tokens;
+  a.workspace_bytes = workspace_bytes;
+  const FusedStats fs = fused_stats(h->impl, a);
+  return fs.on ? fs.layer0 : 0;
 }
 
 int32_t hcr_project_variant(const hcr_handle* h, int32_t n_tokens, int32_t n_layers) {

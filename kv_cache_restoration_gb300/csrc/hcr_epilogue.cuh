@@ -49,6 +49,18 @@ __device__ __forceinline__ int64_t round_tile(int64_t k, int64_t unit, int64_t u
   return k * units + (unit + k) % units;
 }
 
+// Token of TMEM lane `row` (0..127) of this CTA in tile c: a full tile's
+// lane is the CTA's token row; a half tail tile's CTA holds 64 rows, each in
+// two lanes (row % 64).
+template <bool PAIR, bool HT>
+__device__ __forceinline__ int tile_token(const ProjectParams& p, const TileCoord& c,
+                                          uint32_t rank, int row) {
+  constexpr int kTileM = PAIR ? 2 * kBlockM : kBlockM;
+  const bool half_tile = HT && c.m == p.m_tiles - 1;
+  return c.m * kTileM +
+         (half_tile ? int(rank) * (kBlockM / 2) + (row & 63) : int(rank) * kBlockM + row);
+}
+
 // Epilogue of one finished tile, run by each of the four epilogue warps of a
 // CTA on its 32-lane TMEM quadrant `quad` (tacc: the accumulator's TMEM
 // address with the quadrant's lane offset).
@@ -61,14 +73,12 @@ template <int DT, bool PAIR, bool HT>
 __device__ __forceinline__ void token_tile_epilogue(const ProjectParams& p, const TileCoord& c,
                                                     uint32_t rank, int quad, int lane,
                                                     uint32_t tacc) {
-  constexpr int kTileM = PAIR ? 2 * kBlockM : kBlockM;
   const int row = quad * 32 + lane;   // token row within this CTA's 128 rows
   const int half = p.head_dim >> 1;
   const bool half_tile = HT && c.m == p.m_tiles - 1;
   const int col_lo = half_tile ? (row >> 6) * (kBlockN / 2) : 0;
   const int col_hi = half_tile ? col_lo + kBlockN / 2 : kBlockN;
-  const int t = c.m * kTileM +
-                (half_tile ? int(rank) * (kBlockM / 2) + (row & 63) : int(rank) * kBlockM + row);
+  const int t = tile_token<PAIR, HT>(p, c, rank, row);
   bool valid = t < p.n_tokens;
   int64_t slot = -1;
   int pos = 0;
@@ -77,8 +87,10 @@ __device__ __forceinline__ void token_tile_epilogue(const ProjectParams& p, cons
     slot = __ldg(p.slot + t);
     pos = __ldg(p.pos + t);
     const int64_t srow = int64_t(c.l) * p.n_tokens + t;
-    rstd = __ldg(p.rstd + srow);
-    if (p.layer_norm) mean = __ldg(p.mean + srow);
+    // written in this kernel by other CTAs when the statistics are fused:
+    // read through L2, after the wait for their flag
+    rstd = __ldcg(p.rstd + srow);
+    if (p.layer_norm) mean = __ldcg(p.mean + srow);
   }
   valid = valid && slot >= 0;
   const float* csum = p.layer_norm ? p.col_sum + int64_t(c.l) * p.n_cols : nullptr;

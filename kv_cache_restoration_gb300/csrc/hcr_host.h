@@ -71,6 +71,10 @@ cudaError_t launch_kv_rows(const KvRowsParams& p, bool to_cache, int num_sms, cu
 // names `what` when the device cannot address it.
 hcr_status device_view(const Handle& H, void* ptr, const char* what, void** out);
 
+// The smallest workspace a restore of n_tokens tokens over n_layers layers
+// accepts (hcr_workspace_bytes adds the fused statistics' flags to it).
+size_t workspace_min_bytes(const hcr_handle* h, int32_t n_tokens, int32_t n_layers);
+
 // Pieces of hcr_restore for the layer-pipelined restores (hcr_streamed.cu);
 // arguments as in hcr_restore.
 //   pipeline_placement: checks a whole call's arguments (`staging` stands for

@@ -28,8 +28,11 @@ constexpr int kAccums = 2;             // TMEM accumulators (epilogue overlaps n
 constexpr int kTileBytesA = kBlockM * kBlockK * 2;
 constexpr int kTileBytesB = kBlockN * kBlockK * 2;
 constexpr int kStageBytes = kTileBytesA + kTileBytesB;
-constexpr int kProjectThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kEpilogueWarps = 4;
+constexpr int kStatsWarps = 4;         // fused norm statistics
+// warp 0 TMA, warp 1 MMA, warps 2..5 epilogue, warps 6..9 statistics
+constexpr int kProjectThreads = 32 * (2 + kEpilogueWarps + kStatsWarps);
+constexpr int kStatsItemRows = 16;     // tokens per statistics item (one flag)
 constexpr int kGroupM = 16;            // m-tiles per raster group (L2 reuse of hidden rows)
 // dynamic shared memory of each variant's ring + slack to align it to 1024 bytes
 constexpr size_t kSmemSingle = size_t(kStages) * kStageBytes + 1024;
@@ -73,6 +76,7 @@ enum : uint32_t {
   kWaitCodesEmpty = 8,      // encoded input: code producer, a, b = tile, k-block
   kWaitConvCodes = 9,       // encoded input: converter waits for codes, a, b = tile, k-block
   kWaitConvStage = 10,      // encoded input: converter waits for a free A stage
+  kWaitStats = 11,          // epilogue waits for fused statistics, a, b = tile, item
 };
 
 // tcgen05 instruction descriptor for kind::f16, fp32 accumulate, both
@@ -89,6 +93,10 @@ constexpr uint32_t make_idesc_f16(int dtype, int m, int n) {
 // ---------------------------------------------------------------------------
 struct WorkspaceLayout {
   size_t slot_off, pos_off, rstd_off, mean_off, anchor_off, total;
+  // After `total` (the minimum), room for the fused statistics' flags, one
+  // int32 per kStatsItemRows tokens per layer: a workspace of total_fused
+  // bytes lets the token-row projection compute most layers' statistics.
+  size_t flags_off, total_fused;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -110,6 +118,12 @@ inline WorkspaceLayout workspace_layout(int64_t n_tokens, int64_t n_layers, bool
   w.anchor_off = off;
   if (encoded) off = align_up(off + size_t(n_tokens) * 4, 256);
   w.total = off;
+  w.flags_off = off;
+  if (!encoded && n_layers > 0)
+    off = align_up(off + size_t(n_layers) *
+                             size_t((n_tokens + kStatsItemRows - 1) / kStatsItemRows) * 4,
+                   256);
+  w.total_fused = off;
   return w;
 }
 
@@ -158,6 +172,8 @@ struct PrepareParams {
   int32_t skip_placement;   // statistics only (the slot map is written elsewhere)
   int32_t layer_begin;  // model layer of hidden layer 0 (codec bins)
   CodecInput enc;       // codes != nullptr: statistics of the decoded rows
+  int32_t* zero_flags;  // the placement blocks set these n_zero_flags words to 0
+  int64_t n_zero_flags;
 };
 
 struct ProjectParams {
@@ -188,6 +204,16 @@ struct ProjectParams {
   int32_t split_tail;   // the launch's last split_tail tiles run as two half-chunk units
   int32_t stages;   // ring depth (swap_stages(chunk))
   int32_t slot_cols, n_slots;   // TMEM slots: 2 x 256, or 2 big of slot_cols + 1 small
+  // Token-row kernels only, fused norm statistics (stats_flags != nullptr):
+  // the kernel's statistics warps write rstd (and mean) of layers
+  // [stats_layer0, n_layers) from hidden_rows, kStatsItemRows tokens per item,
+  // and set stats_flags[l * stats_items + j] to 1 once item j of layer l is
+  // written; an epilogue waits for the items of its rows first.  Layers below
+  // stats_layer0 come from the prepare kernel.
+  const void* hidden_rows;   // [n_layers][n_tokens][d_model]
+  float eps;
+  int32_t stats_layer0, stats_items;
+  int32_t* stats_flags;
 };
 
 // Launchers (return cudaGetLastError() of the launch).

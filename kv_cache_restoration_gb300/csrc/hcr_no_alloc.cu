@@ -83,7 +83,7 @@ extern "C" hcr_status hcr_restore_no_alloc(hcr_handle* h, const void* hidden, in
                                            void* stream) {
   using namespace hcr;
   if (!h) return set_last_error(HCR_ERR_INVALID_ARG, "handle is NULL");
-  const size_t need = hcr_workspace_bytes(h, n_tokens, layer_end - layer_begin);
+  const size_t need = workspace_min_bytes(h, n_tokens, layer_end - layer_begin);
   if (need > size_t(HCR_NO_ALLOC_SCRATCH_BYTES))
     return set_last_error(HCR_ERR_WORKSPACE,
                           "restore needs %zu bytes of scratch; hcr_restore_no_alloc has %u "

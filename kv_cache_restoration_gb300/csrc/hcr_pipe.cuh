@@ -83,6 +83,27 @@ __device__ __forceinline__ bool wait_phase_sleep(uint32_t bar, uint32_t parity,
   }
 }
 
+// Bounded wait for a flag in global memory that another CTA of the same
+// kernel sets (with a release store) to a non-zero value; the acquire load
+// that sees it orders this thread's later reads after the writer's earlier
+// writes.  Same bound, abort and diagnostics as wait_phase.
+__device__ __forceinline__ bool wait_flag(const int32_t* flag, volatile int32_t* abort,
+                                          const ProjectParams& p, uint32_t code, uint32_t a,
+                                          uint32_t b) {
+  if (ptx::ld_acquire_gpu(flag) != 0) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+    __nanosleep(256);
+    if (ptx::ld_acquire_gpu(flag) != 0) return true;
+    if (*abort) return false;
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      record_timeout(p, code, a, b, 0);
+      return false;
+    }
+  }
+}
+
 // Bounded wait used only while shutting down after an abort.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = ptx::globaltimer_ns();

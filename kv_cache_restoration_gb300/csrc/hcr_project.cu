@@ -40,6 +40,7 @@
 #include <cuda_fp16.h>
 
 #include "hcr_epilogue.cuh"
+#include "hcr_stats.cuh"
 #include "hcr_internal.h"
 #include "hcr_pipe.cuh"
 #include "ptx.cuh"
@@ -245,7 +246,7 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
         ptx::mma_commit(ptx::smem_u32(&ps.drain));
       drain_wait(ptx::smem_u32(&ps.drain), 0);
     }
-  } else {
+  } else if (warp < 2 + kEpilogueWarps) {
     // ------------------------------------------------------------- epilogue
     const int quad = warp & 3;               // TMEM lanes [32*quad, 32*quad+32)
     int acc = 0;
@@ -258,6 +259,16 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
                         uint32_t(tile), uint32_t(acc));
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
+      if (p.stats_flags && c.l >= p.stats_layer0) {
+        // this lane's row statistics come from a statistics item of this
+        // kernel: wait (bounded) until its flag is set
+        const int t = tile_token<PAIR, HT>(p, c, rank, quad * 32 + lane);
+        const int item = t / kStatsItemRows;
+        const bool got = t >= p.n_tokens ||
+                         wait_flag(p.stats_flags + int64_t(c.l) * p.stats_items + item, abort, p,
+                                   kWaitStats, uint32_t(tile), uint32_t(item));
+        if (!__all_sync(0xffffffffu, got)) break;
+      }
       ptx::tc_fence_after();
 
       token_tile_epilogue<DT, PAIR, HT>(
@@ -275,6 +286,34 @@ __global__ void __launch_bounds__(kProjectThreads, 1)
         acc = 0;
         acc_phase ^= 1u;
       }
+    }
+  } else if (p.stats_flags) {
+    // ------------------------------------------------------------- statistics
+    // Norm statistics of layers [stats_layer0, n_layers), kStatsItemRows
+    // tokens per item, items in layer order over every statistics warp of the
+    // grid; each item's flag is set once its rows are written.  These warps
+    // wait for nothing.
+    PrepareParams sp{};
+    sp.hidden = p.hidden_rows;
+    sp.n_tokens = p.n_tokens;
+    sp.d_model = p.d_model;
+    sp.layer_norm = p.layer_norm;
+    sp.dtype = p.dtype;
+    sp.eps = p.eps;
+    sp.rstd = const_cast<float*>(p.rstd);
+    sp.mean = const_cast<float*>(p.mean);
+    const int64_t gw = int64_t(blockIdx.x) * kStatsWarps + (warp - 2 - kEpilogueWarps);
+    const int64_t nw = int64_t(gridDim.x) * kStatsWarps;
+    const int64_t items = int64_t(p.n_layers - p.stats_layer0) * p.stats_items;
+    for (int64_t it = gw; it < items && !*abort; it += nw) {
+      const int l = p.stats_layer0 + int(it / p.stats_items);
+      const int j = int(it - int64_t(l - p.stats_layer0) * p.stats_items);
+      const int t1 = min((j + 1) * kStatsItemRows, p.n_tokens);
+      for (int t = j * kStatsItemRows; t < t1; ++t)
+        stats::row_stats<DT, false>(sp, int64_t(l) * p.n_tokens + t, lane);
+      __syncwarp();
+      if (lane == 0)   // after lane 0's own writes of the item's statistics
+        ptx::st_release_gpu(p.stats_flags + int64_t(l) * p.stats_items + j, 1);
     }
   }
 

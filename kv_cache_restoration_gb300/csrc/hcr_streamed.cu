@@ -244,7 +244,7 @@ hcr_status hidden_pipeline(hcr_handle* h, int32_t layer_begin, int32_t layer_end
   const size_t slot_bytes = size_t(chunk) * size_t(n_tokens) * size_t(h->impl.dims.d_model) * 2;
   return run_pipeline(h, items, slot_bytes, layer_begin, n_req, n_tokens, cu_seqlens, start_pos,
                       block_table, max_blocks_per_req, k_cache, v_cache, layout, staging,
-                      staging_bytes, hcr_workspace_bytes(h, n_tokens, chunk), workspace,
+                      staging_bytes, workspace_min_bytes(h, n_tokens, chunk), workspace,
                       workspace_bytes, stream, copy_item);
 }
 
@@ -428,7 +428,7 @@ extern "C" hcr_status hcr_restore_streamed_split(
   return run_pipeline(
       h, items, slot_bytes, layer_begin, n_req, n_tokens, cu_seqlens, start_pos, block_table,
       max_blocks_per_req, k_cache, v_cache, layout, staging, staging_bytes,
-      hcr_workspace_bytes(h, n_tokens, std::max(ch, 1)), workspace, workspace_bytes, stream,
+      workspace_min_bytes(h, n_tokens, std::max(ch, 1)), workspace, workspace_bytes, stream,
       [&](const Item& it, void* dst, cudaStream_t copy) {
         if (it.kv)
           return copy_status(cudaMemcpyAsync(dst, kv + size_t(it.l0 - n_hid) * kv_layer,
@@ -492,7 +492,7 @@ extern "C" hcr_status hcr_restore_streamed_encoded(
   return run_pipeline(
       h, items, slot_bytes, layer_begin, n_req, n_tokens, cu_seqlens, start_pos, block_table,
       max_blocks_per_req, k_cache, v_cache, layout, staging, staging_bytes,
-      hcr_workspace_bytes(h, n_tokens, chunk), workspace, workspace_bytes, stream,
+      workspace_min_bytes(h, n_tokens, chunk), workspace, workspace_bytes, stream,
       [&](const Item& it, void* dst, cudaStream_t copy) {
         uint8_t* slot = static_cast<uint8_t*>(dst);
         cudaError_t e = cudaMemcpyAsync(slot, codes + size_t(it.l0) * T * dm,

@@ -388,3 +388,47 @@ def test_pair_rounds_with_half_tails(cuda_device, n_tokens):
     Hn.run(b)
     for c in ("k_cache", "v_cache"):
         assert torch.equal(getattr(a, c).view(torch.int16), getattr(b, c).view(torch.int16)), c
+
+
+# Norm statistics fused into the token-row projection: the same bits as the
+# prepare kernel's.  Each case runs twice on the same inputs: with the
+# workspace hcr_workspace_bytes asks for (the projection's statistics warps
+# compute layers L0.. and each epilogue waits for its rows' flags) and with one
+# byte less (the prepare kernel computes every layer).  Cases: CTA pairs with
+# a half tail tile, pairs with a 232-row last tile, single CTAs with
+# LayerNorm, fp16 and K/V bias, and a ragged GQA batch.
+FUSED_CASES = [
+    (W("fused-pairs-ht", ModelShape("fh", 6, 512, 32, 32, 128), [794], [0]), 2),
+    (W("fused-pairs", ModelShape("fp", 6, 512, 32, 32, 128), [1000], [7],
+       block_order="shuffled"), 2),
+    (W("fused-single-ln", ModelShape("fs", 10, 512, 32, 32, 128, norm="ln", dtype="fp16",
+                                     kv_bias=True), [130, 70], [0, 33]), 1),
+    (W("fused-gqa", ModelShape("fg", 8, 1024, 64, 16, 128), [300, 5, 411, 64], [3, 0, 40, 9],
+       block_order="shuffled"), 2),
+]
+
+
+@pytest.mark.parametrize("w,variant", FUSED_CASES, ids=[c[0].name for c in FUSED_CASES])
+def test_fused_statistics_match_prepare(cuda_device, w, variant):
+    from kv_cache_restoration_gb300 import binding as B
+    s = w.shape
+    T = w.n_tokens
+    a = Hn.make_case(w, cuda_device)
+    assert B.hcr_debug_set_variant(a.restorer.handle, variant) == 0
+    ws = a.restorer.workspace(T, s.n_layers, cuda_device)
+    layer0 = B.hcr_debug_fused_stats(a.restorer.handle, T, s.n_layers, ws.numel())
+    assert 1 <= layer0 < s.n_layers, layer0
+    assert B.hcr_debug_fused_stats(a.restorer.handle, T, s.n_layers, ws.numel() - 1) == 0
+    lay = a.layout
+    a.restorer.restore(a.hidden, 0, s.n_layers, a.cu, a.start, a.table, a.k_cache, a.v_cache,
+                       lay.num_blocks, lay.block_size, workspace=ws)
+    a.status, a.flags = a.restorer.check()
+    assert a.status == 0, (a.status, a.flags)
+    Hn.compare(a)
+    b = Hn.make_case(w, cuda_device, params=a.params, restorer=a.restorer)
+    b.restorer.restore(b.hidden, 0, s.n_layers, b.cu, b.start, b.table, b.k_cache, b.v_cache,
+                       lay.num_blocks, lay.block_size, workspace=ws[:ws.numel() - 1])
+    b.status, b.flags = b.restorer.check()
+    assert b.status == 0, (b.status, b.flags)
+    for c in ("k_cache", "v_cache"):
+        assert torch.equal(getattr(a, c).view(torch.int16), getattr(b, c).view(torch.int16)), c

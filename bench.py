@@ -110,6 +110,7 @@ class ClockSampler:
 
 KERNEL_SOURCES = ["kv_cache_restoration_gb300/csrc/hcr_project.cu",
                   "kv_cache_restoration_gb300/csrc/hcr_epilogue.cuh",
+                  "kv_cache_restoration_gb300/csrc/hcr_stats.cuh",
                   "kv_cache_restoration_gb300/csrc/hcr_pipe.cuh",
                   "kv_cache_restoration_gb300/csrc/ptx.cuh",
                   "kv_cache_restoration_gb300/csrc/hcr_internal.h"]

@@ -16,14 +16,18 @@
 // every request's tokens along M: tiles are full except the very last one,
 // whatever the request lengths.
 //
-// Warp roles (192 threads, one CTA per SM):
+// Warp roles (320 threads, one CTA per SM):
 //   warp 0      one lane issues TMA loads of hidden and weight tiles into a
 //               shared-memory ring;
 //   warp 1      allocates TMEM (2 accumulators x 256 fp32 columns) and one
 //               lane issues tcgen05.mma (K=16) for each stage;
 //   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (each warp
 //               owns one 32-lane TMEM quadrant = 32 tokens), overlapping the
-//               MMA of the next tile into the other accumulator.
+//               MMA of the next tile into the other accumulator;
+//   warps 6..9  when the host fuses the norm statistics into the call: the
+//               statistics of layers the prepare kernel left out, 16 tokens
+//               per item, each item's flag set once written; an epilogue
+//               waits (bounded) for its rows' flags.  Otherwise idle.
 // Two variants: single CTAs with 128x256 tiles (cta_group::1, 4 stages of
 // 48 KB), and CTA pairs with 256x256 tiles (cta_group::2, 7 stages of 32 KB
 // per CTA).  The pair halves each SM's share of the weight tile, which cuts

@@ -116,21 +116,33 @@ KERNEL_SOURCES = ["kv_cache_restoration_gb300/csrc/hcr_project.cu",
                   "kv_cache_restoration_gb300/csrc/hcr_internal.h"]
 
 
+def kernel_source_hash() -> str:
+    """Hash of the project kernel's sources with comments and whitespace
+    removed: an edit of a comment leaves the record valid, any code change
+    does not."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for src in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, src)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic(workload_base: str, n_layers: int):
     """DRAM bytes per project launch from the committed ncu record, scaled by
     layers; None if the kernel source changed since the capture or the record
     is for another workload shape."""
-    import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "project_kernel_traffic.json")) as f:
             rec = json.load(f)
-        h = hashlib.sha256()
-        for src in KERNEL_SOURCES:
-            with open(os.path.join(ROOT, src), "rb") as f:
-                h.update(f.read())
+        digest = kernel_source_hash()
     except OSError:
         return None
-    if (rec.get("source_sha256_16") != h.hexdigest()[:16]
+    if (rec.get("source_sha256_16") != digest
             or rec.get("workload_base") != workload_base):
         return None
     return (rec["dram_bytes_read"] + rec["dram_bytes_write"]) * n_layers / rec["captured_layers"]

@@ -180,12 +180,16 @@ hcr_status hcr_restore(hcr_handle* h, const void* hidden, int32_t layer_begin,
 
 /*
  * hcr_restore_prepare / hcr_restore_project -- the two stages of hcr_restore,
- * with identical arguments.  prepare maps every token to its (position,
- * slot) and computes each (layer, token) row's norm statistics into the
- * workspace; project runs the fused K||V GEMM with the norm, bias, RoPE,
- * cast and paged scatter in its epilogue, reading that workspace.  Calling
- * prepare then project on one stream with the same arguments is exactly
- * hcr_restore; splitting them lets a caller time or overlap the stages.
+ * with identical arguments (workspace and workspace_bytes included).  prepare
+ * maps every token to its (position, slot) and computes the (layer, token)
+ * rows' norm statistics into the workspace; project runs the fused K||V GEMM
+ * with the norm, bias, RoPE, cast and paged scatter in its epilogue, reading
+ * that workspace.  When the call fuses the statistics (hcr_debug_fused_stats)
+ * prepare computes only the first layers' and clears the flags, and project
+ * computes the rest; both stages decide that from the same arguments, so they
+ * must be the same.  Calling prepare then project on one stream with the same
+ * arguments is exactly hcr_restore; splitting them lets a caller time or
+ * overlap the stages.
  */
 hcr_status hcr_restore_prepare(hcr_handle* h, const void* hidden, int32_t layer_begin,
                                int32_t layer_end, int32_t n_req, int32_t n_tokens,

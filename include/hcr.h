@@ -560,8 +560,9 @@ hcr_status hcr_restore_no_alloc(hcr_handle* h, const void* hidden, int32_t layer
  * (tokens padded to a multiple of 16 instead of 128 rows; 128-wide heads
  * only).  Host-only; 0 for a NULL handle or empty sizes.  The choice, made
  * from measurements on GB300: 3 for 257..320 tokens; otherwise pairs when
- * there is more than one 128-row tile of tokens, d_model <= 4096 (or at
- * most 512 tokens that leave the pairs no half tail tile), padding to
+ * there is more than one 128-row tile of tokens, d_model <= 4096 (or, for
+ * wider models, a call of at most 6.5 TFLOP that leaves the pairs no half
+ * tail tile), padding to
  * 128-row tiles saves less than 10% of the rows that 256-row tiles pad, and
  * the call is at most 32 TFLOP (4 d_model d_kv n_tokens n_layers); single
  * CTAs otherwise.  hcr_debug_set_variant overrides it.

@@ -284,15 +284,17 @@ struct VariantPolicy {
   int32_t pair_min_tokens = kBlockM + 1;
   // Widths above 4096: single CTAs ran 4-5% faster on the 13B (5120) and
   // OPT-30B (7168) shapes in long power-capped restores and no slower at
-  // 2-4K tokens; at 4096 the pairs win by 5-7%.  Up to pair_wide_max_tokens
-  // tokens, when the pairs need no half tail tile, the pairs win at those
-  // widths too (project ms, single against pairs: 13B 256 tokens 0.855/0.749,
-  // 512 1.524/1.387; OPT-30B 256 tokens 2.064/1.884, 512 3.666/3.506).  With
-  // a half tail they lose at OPT-30B's width (384 tokens 2.888/3.136, 640
-  // 4.511/4.951, 794 5.993/6.510); 13B's pairs win from 768 to 1536 tokens
-  // (2.146/2.000 ... 4.080/3.988) and tie at 2048, not used here.
+  // 2-4K tokens; at 4096 the pairs win by 5-7%.  In calls of at most
+  // pair_wide_max_call_flops, when the pairs need no half tail tile, the pairs
+  // win at those widths too (project ms, single against pairs: 13B 256 tokens
+  // 0.855/0.749, 512 1.524/1.387, 768 2.147/2.000, 1024 2.865/2.708, 1280
+  // 3.452/3.358, 1536 4.080/3.988; OPT-30B 256 tokens 2.064/1.884, 512
+  // 3.666/3.506).  Above that the power cap makes them tie or lose (13B 2048
+  // tokens, 8.6 TFLOP: 5.386/5.378; OPT-30B 768, 7.6 TFLOP: 5.40/5.41; 1024
+  // 7.02/7.14; 1536 10.18/10.71), and with a half tail they lose at OPT-30B's
+  // width (384 tokens 2.888/3.136, 640 4.511/4.951, 794 5.993/6.510).
   int32_t pair_max_d_model = 4096;
-  int32_t pair_wide_max_tokens = 512;
+  double pair_wide_max_call_flops = 6.5e12;
   // Calls above 32 TFLOP (4 d_model d_kv tokens layers): pairs draw more power
   // per clock and the cap pulls their clock down (629K tokens in 8-layer calls
   // of 338 TFLOP: single CTAs 10% faster; 35 TFLOP: a tie; 8.8: pairs 5.5%).
@@ -331,7 +333,8 @@ bool use_pairs(const Handle& H, int32_t n_tokens, int32_t n_layers) {
   const double call_flops = 4.0 * d.d_model * double(d_kv) * double(n_tokens) * n_layers;
   bool pair = H.pair_clusters > 0 && n_tokens >= kPolicy.pair_min_tokens &&
               (d.d_model <= kPolicy.pair_max_d_model ||
-               (n_tokens <= kPolicy.pair_wide_max_tokens && !half_tail_fits(d, n_tokens))) &&
+               (call_flops <= kPolicy.pair_wide_max_call_flops &&
+                !half_tail_fits(d, n_tokens))) &&
               double(pad128) > kPolicy.pair_pad_ratio * double(pad_pair) &&
               call_flops <= kPolicy.pair_max_call_flops;
   if (H.variant == 1) pair = false;

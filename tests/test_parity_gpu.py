@@ -316,13 +316,15 @@ def test_variant_policy_decisions(cuda_device):
     r13 = handle(LLAMA2_13B)
     assert B.hcr_project_variant(r13.handle, 4096, 40) == 1     # d_model 5120
     assert B.hcr_project_variant(r13.handle, 300, 40) == 3
-    # short restores of the wider models: pairs up to 512 tokens, unless the
+    # shorter calls of the wider models: pairs up to 6.5 TFLOP, unless the
     # pairs would end in a half tail tile
     assert B.hcr_project_variant(r13.handle, 256, 40) == 2
     assert B.hcr_project_variant(r13.handle, 512, 40) == 2
     assert B.hcr_project_variant(r13.handle, 400, 40) == 2
-    assert B.hcr_project_variant(r13.handle, 384, 40) == 1
-    assert B.hcr_project_variant(r13.handle, 513, 40) == 1
+    assert B.hcr_project_variant(r13.handle, 1536, 40) == 2      # 6.4 TFLOP
+    assert B.hcr_project_variant(r13.handle, 384, 40) == 1       # half tail
+    assert B.hcr_project_variant(r13.handle, 513, 40) == 1       # half tail
+    assert B.hcr_project_variant(r13.handle, 2048, 40) == 1      # 8.6 TFLOP
     assert B.hcr_debug_set_variant(h, 3) == 0
     assert B.hcr_project_variant(h, 4096, 32) == 3
 

@@ -70,3 +70,27 @@ def test_ragged_batch_in_layer_windows(cuda_device):
         assert case.status == 0, (case.status, case.flags)
         Hn.compare(case, rows=rows, check_sentinel=True)
         del case
+
+
+@pytest.mark.parametrize("name,variant", [("llama2-13b-T1024", 2), ("llama2-13b-T2048", 1),
+                                          ("opt-30b-T512", 2), ("opt-30b-T384", 1)])
+def test_full_width_mid_restores(cuda_device, name, variant):
+    """Mid-size restores of the wider models at full size, in the variant the
+    automatic choice takes for them (CTA pairs for calls of at most 6.5 TFLOP
+    without a half tail tile, single CTAs otherwise; the norm statistics fused
+    into the projection where it has at most 8 m-tiles per layer): every row
+    of the last layer, a seeded row sample of every layer, the sentinel check
+    on every slot."""
+    from kv_cache_restoration_gb300 import binding as B
+    w = C.get(name)
+    L = w.shape.n_layers
+    case = Hn.make_case(w, cuda_device, gen_device=cuda_device)
+    assert B.hcr_project_variant(case.restorer.handle, w.n_tokens, L) == variant
+    lay = case.layout
+    for stage in ("prepare", "project"):
+        case.restorer.restore(case.hidden, 0, L, case.cu, case.start, case.table, case.k_cache,
+                              case.v_cache, lay.num_blocks, lay.block_size, stage=stage)
+    case.status, case.flags = case.restorer.check()
+    assert case.status == 0, (case.status, case.flags)
+    Hn.compare(case, layers=[L - 1], check_sentinel=False)
+    Hn.compare(case, rows=Hn.sample_rows(w, 1 / 32), check_sentinel=True)

@@ -582,7 +582,7 @@ def e2e_record(res, key, source, args, world, w):
             "plain_h2d_gbs": res["h2d_gbs"]}
 
 
-# The benchmark spec's targets beside the headline: each workload restored through
+# The target workloads beside the headline: each workload restored through
 # the same two stages, timed the same way (CUDA events on the launching stream,
 # clocks sampled during the timed region).  Steps per workload keep each timed
 # region at a few tenths of a second.  target: the fraction of the roofline's
@@ -1045,7 +1045,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="cut the model to its first N layers (small profiling cases)")
     ap.add_argument("--targets", default="auto",
-                    help="auto: time the north-star target workloads (13B, OPT-30B, short "
+                    help="auto: time the target workloads (13B, OPT-30B, short "
                          "7B restores) after the headline, on one GPU, for the default "
                          "workload; off; or a comma-separated subset of their names")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -414,6 +414,12 @@ FUSED_CASES = [
                                      kv_bias=True), [130, 70], [0, 33]), 1),
     (W("fused-gqa", ModelShape("fg", 8, 1024, 64, 16, 128), [300, 5, 411, 64], [3, 0, 40, 9],
        block_order="shuffled"), 2),
+    # LayerNorm rows with large means and outlier channels (the two-pass
+    # statistics where one pass would cancel)
+    (replace(W("fused-ln-means", ModelShape("fm", 10, 512, 32, 32, 128, norm="ln", dtype="fp16",
+                                            kv_bias=True), [150, 50], [0, 7]),
+             hidden_means=(-50.0, 10.0, 100.0), outlier_channels=(0, 17, 170, 511),
+             outlier_scale=50.0), 1),
 ]
 
 

@@ -625,6 +625,20 @@ int32_t hcr_debug_fused_stats(const hcr_handle* h, int32_t n_tokens, int32_t n_l
                               size_t workspace_bytes);
 
 /*
+ * hcr_debug_plan -- testing hook (host-only: no handle, no CUDA call): the
+ * choices a restore of n_tokens tokens over n_layers layers of a model with
+ * dims *d makes on a device with num_sms SMs, pair_clusters co-resident CTA
+ * pairs of the token-row kernel and swap_clusters of the weight-row kernel
+ * (0: unavailable), with a workspace of workspace_bytes bytes.  Writes
+ * out[2] = {the tile variant hcr_project_variant would report, the layers the
+ * prepare kernel keeps when the statistics are fused (hcr_debug_fused_stats),
+ * else 0}.  HCR_ERR_INVALID_ARG if d or out is NULL.
+ */
+hcr_status hcr_debug_plan(const hcr_model_dims* d, int32_t n_tokens, int32_t n_layers,
+                          int32_t num_sms, int32_t pair_clusters, int32_t swap_clusters,
+                          size_t workspace_bytes, int32_t* out);
+
+/*
  * hcr_debug_swap_plan -- testing hook (host-only, no handle, no CUDA call):
  * the token chunks and TMEM accumulator slots the weight-row tiles (variant
  * 3) would use for a projection of n_tokens tokens.  Writes out[6] = {chunk,

@@ -159,6 +159,9 @@ lib.hcr_debug_timeout_record.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint3
 lib.hcr_debug_timeout_record.restype = ctypes.c_int
 lib.hcr_debug_fused_stats.argtypes = [_vp, _i32, _i32, ctypes.c_size_t]
 lib.hcr_debug_fused_stats.restype = _i32
+lib.hcr_debug_plan.argtypes = [ctypes.POINTER(hcr_model_dims), _i32, _i32, _i32, _i32, _i32,
+                               ctypes.c_size_t, _vp]
+lib.hcr_debug_plan.restype = ctypes.c_int
 lib.hcr_debug_swap_plan.argtypes = [_i32, _vp]
 lib.hcr_debug_swap_plan.restype = ctypes.c_int
 lib.hcr_debug_set_variant.argtypes = [_vp, _i32]
@@ -465,6 +468,18 @@ def hcr_debug_fused_stats(handle, n_tokens: int, n_layers: int, workspace_bytes:
     """0, or the layers the prepare kernel still computes when the projection
     computes the rest of the norm statistics (host-only)."""
     return lib.hcr_debug_fused_stats(handle, n_tokens, n_layers, workspace_bytes)
+
+
+def hcr_debug_plan(dims, n_tokens: int, n_layers: int, num_sms: int, pair_clusters: int,
+                   swap_clusters: int, workspace_bytes: int) -> tuple:
+    """(tile variant, fused statistics' prepare layers or 0) of a restore on a
+    device with the given unit counts (host-only, no handle)."""
+    out = (ctypes.c_int32 * 2)()
+    st = lib.hcr_debug_plan(ctypes.byref(dims), n_tokens, n_layers, num_sms, pair_clusters,
+                            swap_clusters, workspace_bytes, out)
+    if st != 0:
+        raise RuntimeError(hcr_last_error())
+    return int(out[0]), int(out[1])
 
 
 def hcr_debug_swap_plan(n_tokens: int) -> dict:

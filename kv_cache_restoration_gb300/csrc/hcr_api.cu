@@ -1026,6 +1026,29 @@ hcr_status hcr_debug_swap_plan(int32_t n_tokens, int32_t* out) {
   return HCR_OK;
 }
 
+hcr_status hcr_debug_plan(const hcr_model_dims* d, int32_t n_tokens, int32_t n_layers,
+                          int32_t num_sms, int32_t pair_clusters, int32_t swap_clusters,
+                          size_t workspace_bytes, int32_t* out) {
+  if (!d || !out) return fail(HCR_ERR_INVALID_ARG, "dims and out must be non-NULL");
+  out[0] = out[1] = 0;
+  if (n_tokens <= 0 || n_layers <= 0) return HCR_OK;
+  Handle H{};
+  H.dims = *d;
+  H.num_sms = num_sms;
+  H.pair_clusters = pair_clusters;
+  // as hcr_create: the weight-row tiles take 128-wide heads and need the pairs
+  H.swap_clusters = (d->head_dim == 128 && pair_clusters > 0) ? swap_clusters : 0;
+  out[0] = choose_variant(H, n_tokens, n_layers);
+  RestoreArgs a{};
+  a.layer_begin = 0;
+  a.layer_end = n_layers;
+  a.n_tokens = n_tokens;
+  a.workspace_bytes = workspace_bytes;
+  const FusedStats fs = fused_stats(H, a);
+  out[1] = fs.on ? fs.layer0 : 0;
+  return HCR_OK;
+}
+
 int32_t hcr_debug_fused_stats(const hcr_handle* h, int32_t n_tokens, int32_t n_layers,
                               size_t workspace_bytes) {
   if (!h || n_tokens <= 0 || n_layers <= 0) return 0;
